@@ -1,0 +1,271 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each test checks the oracle (both its recurrent and its chunked routine)
+against something the pages or plain mathematics fix:
+  * a hand-worked two-token example of the gated delta rule,
+  * brute-force evaluation through explicit transition-matrix products,
+  * closed forms (beta = 0, T = 1, orthonormal keys with beta = 1),
+  * exact equality of the recurrent and chunk forms for several chunk sizes
+    (the chunk form with C = 1 is the recurrence; C = L the parallel form),
+  * split/resume, GVA head replication and sequence permutation invariants,
+  * planted mistakes: an oracle with a dropped term or a wrong order fails.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rand_inputs(seed, lengths, hq, hv, dk, dv, s0=True, g_mu=0.0):
+    rng = np.random.default_rng(seed)
+    T = int(sum(lengths))
+    unit = lambda x: x / np.linalg.norm(x, axis=-1, keepdims=True)
+    q = unit(rng.standard_normal((T, hq, dk)))
+    k = unit(rng.standard_normal((T, hq, dk)))
+    v = rng.standard_normal((T, hv, dv))
+    g = -np.logaddexp(0, rng.standard_normal((T, hv)) + g_mu)
+    beta = 1 / (1 + np.exp(-rng.standard_normal((T, hv))))
+    S0 = 0.1 * rng.standard_normal((len(lengths), hv, dk, dv)) if s0 else None
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    return q, k, v, g, beta, S0, cu
+
+
+def rel(a, b):
+    return np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-300)
+
+
+# --------------------------------------------------------------------------
+# hand-worked example (golden fixture, derivation in the file)
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("routine", ["recurrent", "chunked1", "chunked2", "chunked64"])
+def test_hand_example(routine):
+    ex = json.load(open(os.path.join(GOLDEN, "hand_example_T2.json")))
+    i = ex["inputs"]
+    q = np.array(i["q"])[:, None, :]
+    k = np.array(i["k"])[:, None, :]
+    v = np.array(i["v"])[:, None, :]
+    g = np.log(np.array(i["alpha"]))[:, None]
+    beta = np.array(i["beta"])[:, None]
+    cu = [0, 2]
+    if routine == "recurrent":
+        o, S = oracle.recurrent(q, k, v, g, beta, i["scale"], cu_seqlens=cu)
+    else:
+        o, S = oracle.chunked(q, k, v, g, beta, i["scale"], cu_seqlens=cu, chunk_size=int(routine[7:]))
+    np.testing.assert_allclose(o[:, 0, :], ex["expected"]["o"], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(S[0, 0], ex["expected"]["final_state"], rtol=0, atol=1e-14)
+
+
+# --------------------------------------------------------------------------
+# brute force through transition matrices, tiny sizes
+#   S_t = T_t S_{t-1} + beta_t k_t^T v_t,  T_t = alpha_t (I - beta_t k_t^T k_t)
+#   o_t = scale [q_t P_{t,0} S0 + sum_{i<=t} beta_i (q_t P_{t,i} k_i^T) v_i]
+#   P_{t,i} = T_t ... T_{i+1}
+# --------------------------------------------------------------------------
+def brute_force(q, k, v, g, beta, scale, S0):
+    T, dk = k.shape
+    I = np.eye(dk)
+    Tm = [np.exp(g[t]) * (I - beta[t] * np.outer(k[t], k[t])) for t in range(T)]
+    o = np.zeros((T, v.shape[1]))
+    scores = np.zeros((T, T))
+    for t in range(T):
+        P = I.copy()  # P_{t,t}
+        for i in range(t, -1, -1):
+            scores[t, i] = beta[i] * q[t] @ P @ k[i]
+            P = P @ Tm[i]  # now P_{t,i-1}
+        o[t] = scale * (q[t] @ P @ S0 + scores[t] @ v)
+    # final state through the equivalent transition form of the update
+    Sf = S0.copy()
+    for t in range(T):
+        Sf = Tm[t] @ Sf + beta[t] * np.outer(k[t], v[t])
+    return o, Sf
+
+
+@pytest.mark.parametrize("T,dk,dv,C", [(1, 4, 3, 64), (7, 4, 4, 3), (12, 8, 5, 4), (12, 6, 8, 64)])
+def test_brute_force_tiny(T, dk, dv, C):
+    q, k, v, g, beta, S0, cu = rand_inputs(7 + T, [T], 1, 1, dk, dv)
+    o_bf, S_bf = brute_force(q[:, 0], k[:, 0], v[:, 0], g[:, 0], beta[:, 0], 0.3, S0[0, 0])
+    o_r, S_r = oracle.recurrent(q, k, v, g, beta, 0.3, S0, cu)
+    o_c, S_c = oracle.chunked(q, k, v, g, beta, 0.3, S0, cu, chunk_size=C)
+    for o, S in [(o_r, S_r), (o_c, S_c)]:
+        assert rel(o[:, 0], o_bf) < 1e-12
+        assert rel(S[0, 0], S_bf) < 1e-12
+
+
+# --------------------------------------------------------------------------
+# closed forms
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("C", [1, 5, 64])
+def test_beta_zero_pure_decay(C):
+    """beta = 0: S_T = exp(sum g) S0 and o_t = scale exp(G_t) q_t S0."""
+    q, k, v, g, beta, S0, cu = rand_inputs(3, [45], 2, 4, 8, 6)
+    beta[:] = 0.0
+    G = np.cumsum(g, axis=0)  # [T, Hv]
+    hk = np.arange(4) // 2
+    o_exp = 0.7 * np.exp(G)[:, :, None] * np.einsum("thd,hde->the", q[:, hk], S0[0])
+    S_exp = np.exp(G[-1])[:, None, None] * S0[0]
+    for o, S in [oracle.recurrent(q, k, v, g, beta, 0.7, S0, cu),
+                 oracle.chunked(q, k, v, g, beta, 0.7, S0, cu, chunk_size=C)]:
+        assert rel(o, o_exp) < 1e-12
+        assert rel(S[0], S_exp) < 1e-12
+
+
+def test_single_token_closed_form():
+    """T = 1: S_1 = e^g S0 + beta k^T (v - e^g k S0), o = scale q S_1."""
+    q, k, v, g, beta, S0, cu = rand_inputs(11, [1], 1, 2, 16, 16)
+    for h in range(2):
+        a = math.exp(g[0, h])
+        S1 = a * S0[0, h] + beta[0, h] * np.outer(k[0, 0], v[0, h] - a * k[0, 0] @ S0[0, h])
+        for o, S in [oracle.recurrent(q, k, v, g, beta, 0.5, S0, cu),
+                     oracle.chunked(q, k, v, g, beta, 0.5, S0, cu)]:
+            assert rel(S[0, h], S1) < 1e-13
+            assert rel(o[0, h], 0.5 * q[0, 0] @ S1) < 1e-13
+
+
+@pytest.mark.parametrize("with_s0", [False, True])
+@pytest.mark.parametrize("C", [1, 4, 64])
+def test_orthonormal_keys_overwrite(with_s0, C):
+    """g = 0, beta = 1, orthonormal keys: each key reads back its own value.
+
+    With beta = 1 and a unit key the old prediction is replaced by v exactly,
+    and orthogonal keys do not disturb one another: k_j S_T = v_j for every j.
+    Reading with q_t = k_j (j <= t) returns scale * v_j; with S0 = 0 a query
+    orthogonal to all written keys reads zero.
+    """
+    rng = np.random.default_rng(5)
+    dk, dv, T = 16, 8, 10
+    Qm, _ = np.linalg.qr(rng.standard_normal((dk, dk)))
+    keys = Qm[:T]
+    k = keys[:, None, :]
+    v = rng.standard_normal((T, 1, dv))
+    g = np.zeros((T, 1))
+    beta = np.ones((T, 1))
+    S0 = rng.standard_normal((1, 1, dk, dv)) if with_s0 else None
+    js = rng.integers(0, np.arange(1, T + 1))  # j <= t
+    q = keys[js][:, None, :]
+    for o, S in [oracle.recurrent(q, k, v, g, beta, 0.5, S0, [0, T]),
+                 oracle.chunked(q, k, v, g, beta, 0.5, S0, [0, T], chunk_size=C)]:
+        np.testing.assert_allclose(keys @ S[0, 0], v[:, 0], atol=1e-12)
+        np.testing.assert_allclose(o[:, 0], 0.5 * v[js, 0], atol=1e-12)
+        if not with_s0:
+            np.testing.assert_allclose(Qm[T:] @ S[0, 0], 0.0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# recurrent form == chunk form (the pages: C = 1 is the recurrence)
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("C", [1, 7, 64, 200])
+def test_chunked_equals_recurrent(C):
+    q, k, v, g, beta, S0, cu = rand_inputs(21, [200], 2, 4, 32, 24)
+    o_r, S_r = oracle.recurrent(q, k, v, g, beta, 0.125, S0, cu)
+    o_c, S_c = oracle.chunked(q, k, v, g, beta, 0.125, S0, cu, chunk_size=C)
+    assert rel(o_c, o_r) < 1e-11
+    assert rel(S_c, S_r) < 1e-11
+
+
+def test_chunked_equals_recurrent_varlen_full_dims():
+    lengths = [0, 1, 63, 64, 65, 130]
+    q, k, v, g, beta, S0, cu = rand_inputs(22, lengths, 1, 2, 128, 128)
+    o_r, S_r = oracle.recurrent(q, k, v, g, beta, 1 / math.sqrt(128), S0, cu)
+    o_c, S_c = oracle.chunked(q, k, v, g, beta, 1 / math.sqrt(128), S0, cu)
+    assert rel(o_c, o_r) < 1e-11
+    assert rel(S_c, S_r) < 1e-11
+    # zero-length sequence: final state is the initial state
+    np.testing.assert_array_equal(S_c[0], S0[0])
+
+
+def test_dense_layout_matches_packed():
+    q, k, v, g, beta, S0, cu = rand_inputs(23, [70, 70], 1, 1, 8, 8)
+    o_p, S_p = oracle.chunked(q, k, v, g, beta, 1.0, S0, cu)
+    shp = lambda x: x.reshape(2, 70, *x.shape[1:])
+    o_d, S_d = oracle.chunked(shp(q), shp(k), shp(v), shp(g), shp(beta), 1.0, S0)
+    np.testing.assert_array_equal(o_d.reshape(o_p.shape), o_p)
+    np.testing.assert_array_equal(S_d, S_p)
+
+
+# --------------------------------------------------------------------------
+# invariants
+# --------------------------------------------------------------------------
+def test_split_resume():
+    """Ch(T1) -> final -> Ch(T2, S0=final) equals Ch(T1+T2)."""
+    q, k, v, g, beta, S0, cu = rand_inputs(31, [150], 1, 2, 16, 16)
+    o_full, S_full = oracle.chunked(q, k, v, g, beta, 0.25, S0, cu)
+    T1 = 71
+    o_a, S_a = oracle.chunked(q[:T1], k[:T1], v[:T1], g[:T1], beta[:T1], 0.25, S0, [0, T1])
+    o_b, S_b = oracle.chunked(q[T1:], k[T1:], v[T1:], g[T1:], beta[T1:], 0.25, S_a, [0, 150 - T1])
+    assert rel(np.concatenate([o_a, o_b]), o_full) < 1e-12
+    assert rel(S_b, S_full) < 1e-12
+
+
+def test_gva_equals_replicated_heads():
+    """Hv = G*Hq with shared q/k equals Hq = Hv with q/k heads repeated."""
+    q, k, v, g, beta, S0, cu = rand_inputs(41, [90], 2, 6, 16, 8)
+    o_g, S_g = oracle.chunked(q, k, v, g, beta, 0.3, S0, cu)
+    rep = lambda x: np.repeat(x, 3, axis=1)
+    o_r, S_r = oracle.chunked(rep(q), rep(k), v, g, beta, 0.3, S0, cu)
+    np.testing.assert_array_equal(o_g, o_r)
+    np.testing.assert_array_equal(S_g, S_r)
+
+
+def test_sequence_permutation():
+    """Reordering packed sequences reorders outputs bit for bit."""
+    lengths = [33, 100, 7, 64]
+    q, k, v, g, beta, S0, cu = rand_inputs(51, lengths, 1, 2, 16, 16)
+    o, S = oracle.chunked(q, k, v, g, beta, 0.3, S0, cu)
+    perm = [2, 0, 3, 1]
+    segs = lambda x: [x[cu[i]:cu[i + 1]] for i in range(4)]
+    cat = lambda x: np.concatenate([segs(x)[p] for p in perm])
+    cu2 = np.concatenate([[0], np.cumsum([lengths[p] for p in perm])])
+    o2, S2 = oracle.chunked(cat(q), cat(k), cat(v), cat(g), cat(beta), 0.3, S0[perm], cu2)
+    np.testing.assert_array_equal(o2, cat(o))
+    np.testing.assert_array_equal(S2, S[perm])
+
+
+def test_recurrent_step_slots():
+    """Decode wrapper: slot gather/scatter, negative index skips."""
+    q, k, v, g, beta, _, _ = rand_inputs(61, [3], 1, 2, 8, 8)
+    state = np.random.default_rng(1).standard_normal((5, 2, 8, 8))
+    idx = np.array([4, -1, 1])
+    o, st = oracle.recurrent_step(q, k, v, g, beta, 0.5, state, idx)
+    o_ref, S_ref = oracle.recurrent(q[[0, 2]], k[[0, 2]], v[[0, 2]], g[[0, 2]], beta[[0, 2]], 0.5,
+                                    state[[4, 1]], [0, 1, 2])
+    np.testing.assert_array_equal(o[[0, 2]], o_ref)
+    np.testing.assert_array_equal(o[1], 0.0)
+    np.testing.assert_array_equal(st[[4, 1]], S_ref)
+    np.testing.assert_array_equal(st[[0, 2, 3]], state[[0, 2, 3]])
+
+
+# --------------------------------------------------------------------------
+# planted mistakes (on the CPU, in a copy of the oracle's arithmetic) must be
+# caught by the hand example: guards the pins themselves
+# --------------------------------------------------------------------------
+def _mutant_recurrent(q, k, v, alpha, beta, mode):
+    S = np.zeros((k.shape[1], v.shape[1]))
+    o = []
+    for t in range(len(k)):
+        if mode == "decay_after_write":
+            S = S + beta[t] * np.outer(k[t], v[t] - k[t] @ S)
+            S = alpha[t] * S
+        elif mode == "read_before_write":
+            S = alpha[t] * S
+            o.append(q[t] @ S)
+            S = S + beta[t] * np.outer(k[t], v[t] - k[t] @ S)
+            continue
+        elif mode == "no_prediction":
+            S = alpha[t] * S + beta[t] * np.outer(k[t], v[t])
+        o.append(q[t] @ S)
+    return np.array(o), S
+
+
+@pytest.mark.parametrize("mode", ["decay_after_write", "read_before_write", "no_prediction"])
+def test_hand_example_catches_planted_mistakes(mode):
+    ex = json.load(open(os.path.join(GOLDEN, "hand_example_T2.json")))
+    i = ex["inputs"]
+    o, S = _mutant_recurrent(np.array(i["q"]), np.array(i["k"]), np.array(i["v"]), i["alpha"], i["beta"], mode)
+    bad = not (np.allclose(o, ex["expected"]["o"]) and np.allclose(S, ex["expected"]["final_state"]))
+    assert bad
