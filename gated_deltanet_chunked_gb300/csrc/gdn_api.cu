@@ -1,0 +1,181 @@
+// C ABI of libgdn.so: argument checks, workspace carving and dispatch.
+//
+// Every entry point validates all of its arguments before the first launch
+// and returns a gdn_status; nothing is enqueued on failure. There is one
+// compute path per io dtype (f32: SIMT kernels; bf16: tensor-core kernels)
+// and no host-side fallback of any kind.
+#include <mutex>
+
+#include "gdn_common.cuh"
+
+namespace gdn {
+namespace {
+
+__device__ int g_status_word;  // device status word (first device-side error)
+
+constexpr int kMaxDevices = 64;
+int *g_status_ptr[kMaxDevices];
+std::mutex g_status_mu;
+
+// Device address of the status word for the current device (looked up once
+// per device; cudaGetSymbolAddress needs that device to be current).
+int *status_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_status_mu);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int *>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Checks shared by prefill and decode. Returns GDN_OK or the error code.
+int check_common(const gdn_problem *p) {
+    if (!p) return GDN_EINVAL;
+    if (p->hq <= 0 || p->hv <= 0 || p->dk <= 0 || p->dv <= 0) return GDN_EINVAL;
+    if (p->hv % p->hq != 0) return GDN_EINVAL;
+    if (p->io_dtype != GDN_DT_F32 && p->io_dtype != GDN_DT_BF16) return GDN_EINVAL;
+    if (p->num_seqs < 0 || p->total_tokens < 0) return GDN_EINVAL;
+    if (p->dk != kHeadDim || p->dv != kHeadDim) return GDN_EUNSUPPORTED;
+    if (p->flags != 0) return GDN_EUNSUPPORTED;
+    return GDN_OK;
+}
+
+int check_prefill_shape(const gdn_problem *p, bool packed) {
+    int st = check_common(p);
+    if (st) return st;
+    if (p->num_seqs < 1) return GDN_EINVAL;
+    if (!packed) {
+        if (p->batch < 1 || p->seqlen < 0 || p->num_seqs != p->batch) return GDN_EINVAL;
+        if (int64_t(p->batch) * p->seqlen != p->total_tokens) return GDN_EINVAL;
+    }
+    // token-row products must stay addressable with 64-bit offsets and the
+    // chunk count must fit the int32 chunk table
+    if (int64_t(p->total_tokens) / kChunk + p->num_seqs > (int64_t(1) << 30)) return GDN_EINVAL;
+    return GDN_OK;
+}
+
+int max_chunks_of(const gdn_problem *p) { return p->total_tokens / kChunk + p->num_seqs; }
+
+// Workspace layout: [n_chunks | seq_info | chunk_info | kernel data].
+struct WsLayout {
+    size_t seq_off, chunk_off, data_off, data_bytes, total;
+};
+
+WsLayout ws_layout(const gdn_problem *p) {
+    WsLayout l;
+    const int mc = max_chunks_of(p);
+    l.seq_off = 256;
+    l.chunk_off = l.seq_off + align256(sizeof(SeqInfo) * size_t(p->num_seqs));
+    l.data_off = l.chunk_off + align256(sizeof(ChunkInfo) * size_t(mc));
+    l.data_bytes = prefill_simt_workspace(mc, p->hv);
+    l.total = l.data_off + l.data_bytes;
+    return l;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ECUDA; }
+
+}  // namespace
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" {
+
+int gdn_version(void) { return 100; }
+
+const char *gdn_status_string(int status) {
+    switch (status) {
+        case GDN_OK: return "GDN_OK";
+        case GDN_EINVAL: return "GDN_EINVAL: invalid argument (pointer, shape, size or alignment)";
+        case GDN_EUNSUPPORTED: return "GDN_EUNSUPPORTED: valid but unsupported (dk/dv must be 128, flags 0)";
+        case GDN_ECUDA: return "GDN_ECUDA: a CUDA runtime call or kernel launch failed";
+        case GDN_ETIMEOUT: return "GDN_ETIMEOUT: a bounded device-side wait gave up";
+        case GDN_EDEVICE_INPUT: return "GDN_EDEVICE_INPUT: device-side input check failed (cu_seqlens or slot index)";
+        default: return "unknown gdn_status";
+    }
+}
+
+size_t gdn_chunk_fwd_workspace_size(const gdn_problem *p) {
+    // the size depends only on total_tokens, num_seqs and hv, so the packed
+    // checks (a superset of nothing layout-specific) are the right ones here
+    if (check_prefill_shape(p, /*packed=*/true) != GDN_OK) return 0;
+    return ws_layout(p).total;
+}
+
+int gdn_chunk_fwd(const gdn_problem *p, const void *q, const void *k, const void *v, const float *g,
+                  const float *beta, float scale, const float *initial_state, const int32_t *cu_seqlens,
+                  void *out, float *final_state, void *workspace, size_t workspace_bytes, void *stream) {
+    const bool packed = cu_seqlens != nullptr;
+    int st = check_prefill_shape(p, packed);
+    if (st) return st;
+    if (p->total_tokens > 0) {
+        if (!q || !k || !v || !g || !beta || !out) return GDN_EINVAL;
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) || !aligned16(out))
+            return GDN_EINVAL;
+    }
+    if ((initial_state && !aligned16(initial_state)) || (final_state && !aligned16(final_state)) ||
+        (cu_seqlens && !aligned16(cu_seqlens)))
+        return GDN_EINVAL;
+    const WsLayout L = ws_layout(p);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < L.total)
+        return GDN_EINVAL;
+    int *status = status_ptr();
+    if (!status) return GDN_ECUDA;
+
+    char *ws = static_cast<char *>(workspace);
+    PrefillArgs a{};
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta;
+    a.s0 = initial_state; a.final_state = final_state; a.out = out; a.scale = scale;
+    a.hq = p->hq; a.hv = p->hv; a.group = p->hv / p->hq;
+    a.num_seqs = p->num_seqs; a.total_tokens = p->total_tokens;
+    a.dense_batch = packed ? 0 : p->batch;
+    a.dense_seqlen = packed ? 0 : p->seqlen;
+    a.cu = cu_seqlens;
+    a.max_chunks = max_chunks_of(p);
+    a.n_chunks = reinterpret_cast<int *>(ws);
+    a.seq_info = reinterpret_cast<SeqInfo *>(ws + L.seq_off);
+    a.chunk_info = reinterpret_cast<ChunkInfo *>(ws + L.chunk_off);
+    a.status = status;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((st = cuda_status(launch_chunk_table(a, s)))) return st;
+    return cuda_status(launch_prefill_simt(a, p->io_dtype == GDN_DT_BF16, ws + L.data_off, s));
+}
+
+int gdn_recurrent_step(const gdn_problem *p, const void *q, const void *k, const void *v, const float *g,
+                       const float *beta, float scale, float *state, const int32_t *state_indices, void *out,
+                       void *stream) {
+    int st = check_common(p);
+    if (st) return st;
+    if (p->total_tokens != p->num_seqs) return GDN_EINVAL;
+    if (p->num_state_slots < 0 || (!state_indices && p->num_state_slots < p->num_seqs)) return GDN_EINVAL;
+    if (p->num_seqs > 0) {
+        if (!q || !k || !v || !g || !beta || !out || !state) return GDN_EINVAL;
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) ||
+            !aligned16(out) || !aligned16(state) || (state_indices && !aligned16(state_indices)))
+            return GDN_EINVAL;
+    }
+    if (int64_t(p->num_seqs) * p->hv >= (int64_t(1) << 31)) return GDN_EINVAL;
+    int *status = status_ptr();
+    if (!status) return GDN_ECUDA;
+    return cuda_status(launch_recurrent_step(*p, q, k, v, g, beta, scale, state, state_indices, out, status,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+int gdn_read_device_status(void *stream, int clear) {
+    int *status = status_ptr();
+    if (!status) return GDN_ECUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int host = 0;
+    if (cudaMemcpyAsync(&host, status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return GDN_ECUDA;
+    if (clear && cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return GDN_ECUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ECUDA;
+    return host;
+}
+
+}  // extern "C"

@@ -1,0 +1,92 @@
+// Shared device-side definitions of libgdn (not part of the public ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gdn.h"
+
+namespace gdn {
+
+constexpr int kChunk = 64;   // chunk size C fixed by the Lab3 GDN Prefill page
+constexpr int kHeadDim = 128;  // d_k = d_v = 128 on every configuration
+
+// One 64-token chunk of one sequence (built on the device from cu_seqlens).
+struct ChunkInfo {
+    int seq;    // sequence index
+    int start;  // first token row of the chunk
+    int len;    // valid length l_c = min(64, L - c*64), 1..64
+    int idx;    // chunk index inside its sequence
+};
+
+// Per-sequence range of chunks in the global chunk list.
+struct SeqInfo {
+    int first_chunk;
+    int num_chunks;
+    int start;  // first token row of the sequence
+    int len;    // tokens in the sequence
+};
+
+// Everything a prefill launch needs; built once on the host per call.
+struct PrefillArgs {
+    const void *q, *k, *v;
+    const float *g, *beta;
+    const float *s0;
+    float *final_state;
+    void *out;
+    float scale;
+    int hq, hv, group;  // group = hv / hq
+    int num_seqs, total_tokens;
+    int dense_batch, dense_seqlen;  // used when cu == nullptr
+    const int *cu;
+    int max_chunks;
+    // workspace regions
+    int *n_chunks;  // [1]
+    SeqInfo *seq_info;  // [num_seqs]
+    ChunkInfo *chunk_info;  // [max_chunks]
+    int *status;  // device status word
+};
+
+__device__ __forceinline__ void record_status(int *status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// Counts a kernel launch and, when profiling is enabled, brackets it with
+// CUDA events on `s` (construct right before the launch, destroy right after).
+class LaunchScope {
+  public:
+    LaunchScope(int kernel, cudaStream_t s);
+    ~LaunchScope();
+    LaunchScope(const LaunchScope &) = delete;
+    LaunchScope &operator=(const LaunchScope &) = delete;
+
+  private:
+    int kernel_;
+    cudaStream_t stream_;
+    cudaEvent_t start_;
+};
+
+// Host-side launchers implemented in the kernel translation units.
+cudaError_t launch_chunk_table(const PrefillArgs &a, cudaStream_t s);
+cudaError_t launch_prefill_simt(const PrefillArgs &a, bool bf16, void *ws_data, cudaStream_t s);
+size_t prefill_simt_workspace(int max_chunks, int hv);
+cudaError_t launch_recurrent_step(const gdn_problem &p, const void *q, const void *k, const void *v,
+                                  const float *g, const float *beta, float scale, float *state,
+                                  const int32_t *state_indices, void *out, int *status, cudaStream_t s);
+
+}  // namespace gdn

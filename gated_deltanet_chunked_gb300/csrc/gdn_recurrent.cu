@@ -1,0 +1,137 @@
+// Single-token recurrent decode step (gdn_recurrent_step).
+//
+// The gated delta rule of the Lab3 GDN Prefill page (section "Linear
+// Attention 与 Gated DeltaNet"), applied once per sequence with the operation
+// order of decode node 7 on the sgl-qwen3-5-moe page: decay the old state,
+// predict with the key, write the beta-weighted correction, read with the
+// query from the UPDATED state.
+//
+// The step is HBM-bound: every (sequence, v-head) streams its 64 KiB f32 state
+// in and out once (2 x 64 KiB per pair, 1.07 GB per step at 256 x 32 pairs).
+// One CTA of 256 threads owns one pair. Thread t holds columns 4*(t%32)..+3 of
+// rows t/32 + 8i (i < 16) as 16 float4 registers, so each warp moves whole
+// 512-byte rows (fully coalesced 128-bit accesses) and the state is read and
+// written exactly once.
+//
+// Both reductions over dk are taken in one pass from the OLD state:
+//   p   = k S_old                    (prediction before decay: k S_bar = alpha p)
+//   r   = q S_old,  qk = q . k
+//   d   = beta (v - alpha p)
+//   o   = scale (alpha r + qk d)     (= scale q (alpha S_old + k^T d) exactly)
+//   S'  = alpha S_old + k^T d
+// so the new state never has to be re-read to produce the output.
+#include "gdn_common.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kRThreads = 256;
+constexpr int kRowsPerThread = kHeadDim / (kRThreads / 32);  // 16
+
+template <typename T>
+__device__ __forceinline__ float ldx(const void *p, size_t i) {
+    return to_f32<T>(static_cast<const T *>(p)[i]);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kRThreads, 2)
+k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const void *__restrict__ v,
+                 const float *__restrict__ g, const float *__restrict__ beta, float scale,
+                 float *__restrict__ state, const int32_t *__restrict__ idx, void *__restrict__ out,
+                 int num_seqs, int hq, int hv, int slots, int *status) {
+    __shared__ float ks[kHeadDim], qs[kHeadDim];
+    __shared__ float4 red_p[kRThreads / 32][32], red_r[kRThreads / 32][32];
+    __shared__ float qk_s;
+    const int pair = blockIdx.x;
+    const int n = pair / hv, h = pair % hv, hk = h / (hv / hq);
+    const int tid = threadIdx.x, lane = tid & 31, wrow = tid >> 5;
+    int slot = idx ? idx[n] : n;
+    if (slot < 0) return;  // padding slot: nothing read, nothing written
+    if (slot >= slots) {
+        if (tid == 0) record_status(status, GDN_EDEVICE_INPUT);
+        return;
+    }
+    float4 *S = reinterpret_cast<float4 *>(state + (size_t(slot) * hv + h) * kHeadDim * kHeadDim);
+    // issue all state loads first: 16 independent 128-bit loads per thread
+    float4 s[kRowsPerThread];
+#pragma unroll
+    for (int i = 0; i < kRowsPerThread; ++i) s[i] = S[(wrow + 8 * i) * 32 + lane];
+    if (tid < kHeadDim) {
+        const size_t qk_off = (size_t(n) * hq + hk) * kHeadDim + tid;
+        ks[tid] = ldx<T>(k, qk_off);
+        qs[tid] = ldx<T>(q, qk_off);
+    }
+    __syncthreads();
+    if (wrow == 0) {  // q . k by warp 0
+        float acc = 0.f;
+        for (int d = lane; d < kHeadDim; d += 32) acc = fmaf(qs[d], ks[d], acc);
+        for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) qk_s = acc;
+    }
+    float4 p = make_float4(0.f, 0.f, 0.f, 0.f), r = p;
+#pragma unroll
+    for (int i = 0; i < kRowsPerThread; ++i) {
+        const float kd = ks[wrow + 8 * i], qd = qs[wrow + 8 * i];
+        p.x = fmaf(kd, s[i].x, p.x); p.y = fmaf(kd, s[i].y, p.y);
+        p.z = fmaf(kd, s[i].z, p.z); p.w = fmaf(kd, s[i].w, p.w);
+        r.x = fmaf(qd, s[i].x, r.x); r.y = fmaf(qd, s[i].y, r.y);
+        r.z = fmaf(qd, s[i].z, r.z); r.w = fmaf(qd, s[i].w, r.w);
+    }
+    red_p[wrow][lane] = p;
+    red_r[wrow][lane] = r;
+    __syncthreads();
+    p = make_float4(0.f, 0.f, 0.f, 0.f);
+    r = p;
+#pragma unroll
+    for (int w = 0; w < kRThreads / 32; ++w) {
+        const float4 a = red_p[w][lane], b = red_r[w][lane];
+        p.x += a.x; p.y += a.y; p.z += a.z; p.w += a.w;
+        r.x += b.x; r.y += b.y; r.z += b.z; r.w += b.w;
+    }
+    const float alpha = expf(g[size_t(n) * hv + h]);
+    const float b = beta[size_t(n) * hv + h];
+    const size_t vo = (size_t(n) * hv + h) * kHeadDim + 4 * lane;
+    float4 d;
+    d.x = b * (ldx<T>(v, vo + 0) - alpha * p.x);
+    d.y = b * (ldx<T>(v, vo + 1) - alpha * p.y);
+    d.z = b * (ldx<T>(v, vo + 2) - alpha * p.z);
+    d.w = b * (ldx<T>(v, vo + 3) - alpha * p.w);
+    if (wrow == 0) {
+        const float qk = qk_s;
+        T *o = static_cast<T *>(out) + vo;
+        o[0] = from_f32<T>(scale * fmaf(alpha, r.x, qk * d.x));
+        o[1] = from_f32<T>(scale * fmaf(alpha, r.y, qk * d.y));
+        o[2] = from_f32<T>(scale * fmaf(alpha, r.z, qk * d.z));
+        o[3] = from_f32<T>(scale * fmaf(alpha, r.w, qk * d.w));
+    }
+#pragma unroll
+    for (int i = 0; i < kRowsPerThread; ++i) {
+        const float kd = ks[wrow + 8 * i];
+        float4 t;
+        t.x = fmaf(alpha, s[i].x, kd * d.x);
+        t.y = fmaf(alpha, s[i].y, kd * d.y);
+        t.z = fmaf(alpha, s[i].z, kd * d.z);
+        t.w = fmaf(alpha, s[i].w, kd * d.w);
+        S[(wrow + 8 * i) * 32 + lane] = t;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_recurrent_step(const gdn_problem &p, const void *q, const void *k, const void *v,
+                                  const float *g, const float *beta, float scale, float *state,
+                                  const int32_t *state_indices, void *out, int *status, cudaStream_t s) {
+    const unsigned pairs = unsigned(p.num_seqs) * unsigned(p.hv);
+    if (pairs == 0) return cudaSuccess;
+    LaunchScope scope(GDN_K_RECURRENT_STEP, s);
+    if (p.io_dtype == GDN_DT_BF16)
+        k_recurrent_step<__nv_bfloat16><<<pairs, kRThreads, 0, s>>>(q, k, v, g, beta, scale, state, state_indices,
+                                                                   out, p.num_seqs, p.hq, p.hv,
+                                                                   p.num_state_slots, status);
+    else
+        k_recurrent_step<float><<<pairs, kRThreads, 0, s>>>(q, k, v, g, beta, scale, state, state_indices, out,
+                                                           p.num_seqs, p.hq, p.hv, p.num_state_slots, status);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

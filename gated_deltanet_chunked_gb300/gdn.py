@@ -1,0 +1,189 @@
+"""Thin ctypes binding of libgdn.so (include/gdn.h).
+
+Argument marshalling only: every step of the forward runs in the library's
+CUDA kernels. PyTorch supplies device memory and the current stream. There is
+no fallback: if libgdn.so cannot be built or loaded, ``load()`` raises.
+
+The entry points keep the C names:
+  gdn_chunk_fwd, gdn_chunk_fwd_workspace_size, gdn_recurrent_step,
+  gdn_read_device_status, gdn_status_string, gdn_version.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+GDN_OK, GDN_EINVAL, GDN_EUNSUPPORTED, GDN_ECUDA, GDN_ETIMEOUT, GDN_EDEVICE_INPUT = range(6)
+GDN_DT_F32, GDN_DT_BF16 = 0, 1
+
+SYMBOLS = ("gdn_chunk_fwd", "gdn_chunk_fwd_workspace_size", "gdn_recurrent_step", "gdn_read_device_status",
+           "gdn_status_string", "gdn_version", "gdn_profile_enable", "gdn_profile_collect", "gdn_kernel_name")
+GDN_K_COUNT = 7
+
+
+class GdnProblem(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("seqlen", ctypes.c_int32), ("num_seqs", ctypes.c_int32),
+                ("total_tokens", ctypes.c_int32), ("hq", ctypes.c_int32), ("hv", ctypes.c_int32),
+                ("dk", ctypes.c_int32), ("dv", ctypes.c_int32), ("io_dtype", ctypes.c_int32),
+                ("flags", ctypes.c_uint32), ("num_state_slots", ctypes.c_int32)]
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {gdn_status_string(status)}")
+
+
+_lib = None
+_lock = threading.Lock()
+_vp, _fp, _ip = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+
+
+def load(path: Optional[str] = None):
+    """Build (if stale) and load libgdn.so; raises if either step fails."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(path or _build.build())
+            P = ctypes.POINTER(GdnProblem)
+            lib.gdn_chunk_fwd.argtypes = [P, _vp, _vp, _vp, _fp, _fp, ctypes.c_float, _fp, _ip, _vp, _fp, _vp,
+                                          ctypes.c_size_t, _vp]
+            lib.gdn_chunk_fwd.restype = ctypes.c_int
+            lib.gdn_chunk_fwd_workspace_size.argtypes = [P]
+            lib.gdn_chunk_fwd_workspace_size.restype = ctypes.c_size_t
+            lib.gdn_recurrent_step.argtypes = [P, _vp, _vp, _vp, _fp, _fp, ctypes.c_float, _fp, _ip, _vp, _vp]
+            lib.gdn_recurrent_step.restype = ctypes.c_int
+            lib.gdn_read_device_status.argtypes = [_vp, ctypes.c_int]
+            lib.gdn_read_device_status.restype = ctypes.c_int
+            lib.gdn_status_string.argtypes = [ctypes.c_int]
+            lib.gdn_status_string.restype = ctypes.c_char_p
+            lib.gdn_version.argtypes = []
+            lib.gdn_version.restype = ctypes.c_int
+            lib.gdn_profile_enable.argtypes = [ctypes.c_int]
+            lib.gdn_profile_enable.restype = ctypes.c_int
+            lib.gdn_profile_collect.argtypes = [_vp, _vp, _vp, ctypes.c_int, ctypes.c_int]
+            lib.gdn_profile_collect.restype = ctypes.c_int
+            lib.gdn_kernel_name.argtypes = [ctypes.c_int]
+            lib.gdn_kernel_name.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def lib():
+    return load()
+
+
+def gdn_status_string(status: int) -> str:
+    return load().gdn_status_string(int(status)).decode()
+
+
+def gdn_version() -> int:
+    return int(load().gdn_version())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("libgdn wants contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _io_dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return GDN_DT_F32
+    if t.dtype == torch.bfloat16:
+        return GDN_DT_BF16
+    raise ValueError(f"unsupported io dtype {t.dtype}")
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def prefill_problem(q: torch.Tensor, v: torch.Tensor, num_seqs: int, packed: bool) -> GdnProblem:
+    """Descriptor for q [T_total, Hq, dk] (packed) or [B, T, Hq, dk] (dense)."""
+    if packed:
+        Ttot, hq, dk = q.shape
+        batch, seqlen = 1, 0
+    else:
+        batch, seqlen, hq, dk = q.shape
+        Ttot = batch * seqlen
+        num_seqs = batch
+    return GdnProblem(batch, seqlen, num_seqs, Ttot, hq, v.shape[-2], dk, v.shape[-1], _io_dtype(q), 0, 0)
+
+
+def gdn_chunk_fwd_workspace_size(problem: GdnProblem) -> int:
+    return int(load().gdn_chunk_fwd_workspace_size(ctypes.byref(problem)))
+
+
+def gdn_chunk_fwd(q, k, v, g, beta, scale, initial_state=None, cu_seqlens=None, out=None,
+                  final_state=None, output_final_state=True, workspace=None, stream=None):
+    """Chunked prefill. Packed when ``cu_seqlens`` (int32 device [N+1]) is given.
+
+    Returns (out, final_state). ``workspace`` (uint8 device tensor) is
+    allocated with PyTorch when not supplied.
+    """
+    packed = cu_seqlens is not None
+    num_seqs = cu_seqlens.numel() - 1 if packed else q.shape[0]
+    prob = prefill_problem(q, v, num_seqs, packed)
+    if out is None:
+        out = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((prob.num_seqs, prob.hv, prob.dk, prob.dv), dtype=torch.float32, device=v.device)
+    need = gdn_chunk_fwd_workspace_size(prob)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=v.device)
+    st = load().gdn_chunk_fwd(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                              ctypes.c_float(scale), _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
+                              _ptr(final_state), _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                              _stream(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_chunk_fwd")
+    return out, final_state
+
+
+def gdn_recurrent_step(q, k, v, g, beta, scale, state, state_indices=None, out=None, stream=None):
+    """One decode step; ``state`` [slots, Hv, 128, 128] f32 is updated in place."""
+    N, hq, dk = q.shape
+    prob = GdnProblem(N, 1, N, N, hq, v.shape[1], dk, v.shape[2], _io_dtype(q), 0, state.shape[0])
+    if out is None:
+        out = torch.empty(v.shape, dtype=v.dtype, device=v.device)
+    st = load().gdn_recurrent_step(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                   ctypes.c_float(scale), _ptr(state), _ptr(state_indices), _ptr(out),
+                                   _stream(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_recurrent_step")
+    return out
+
+
+def gdn_read_device_status(stream=None, clear: bool = True) -> int:
+    return int(load().gdn_read_device_status(_stream(stream), int(clear)))
+
+
+def gdn_profile_enable(enable: bool = True) -> None:
+    load().gdn_profile_enable(int(enable))
+
+
+def gdn_kernel_name(kernel: int) -> str:
+    return load().gdn_kernel_name(int(kernel)).decode()
+
+
+def gdn_profile_collect(reset: bool = True) -> dict:
+    """{kernel name: (launches, summed event ms, timed launches)} for kernels that ran."""
+    n = GDN_K_COUNT
+    launches = (ctypes.c_longlong * n)()
+    ms = (ctypes.c_double * n)()
+    timed = (ctypes.c_longlong * n)()
+    st = load().gdn_profile_collect(ctypes.cast(launches, _vp), ctypes.cast(ms, _vp), ctypes.cast(timed, _vp), n,
+                                    int(reset))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_profile_collect")
+    return {gdn_kernel_name(i): (int(launches[i]), float(ms[i]), int(timed[i])) for i in range(n) if launches[i]}

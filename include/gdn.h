@@ -1,0 +1,179 @@
+/*
+ * gdn.h -- C ABI of libgdn.so: the Gated DeltaNet forward on one NVIDIA
+ * GB300 (sm_103a), chunk-wise parallel prefill and single-token decode step.
+ *
+ * Sources (web pages on Gated DeltaNet):
+ *  [Lab3]  "Lab3 GDN Prefill" (hpc101.zjusct.io).
+ *          Section "Linear Attention 与 Gated DeltaNet": the gated delta rule
+ *            S_t = alpha_t (I - beta_t k_t^T k_t) S_{t-1} + beta_t k_t^T v_t,
+ *            o_t = q_t S_t (row vectors; S is dk x dv).
+ *          Section "计算过程描述": the chunk form with C = 64,
+ *            A = (I + StrictLower(B Gamma K K^T Gamma^-1))^-1,
+ *            U = A B V, W = A B Gamma K,
+ *            S_[c+1] = gamma_l S_[c] + gamma_l K^T Gamma^-1 (U - W S_[c]),
+ *            O_[c] = (1/sqrt dk)[Gamma Q S_[c] + Gamma Lower(Q K^T) Gamma^-1 (U - W S_[c])],
+ *            valid chunk length l_c = min(C, L - cC), tail columns masked.
+ *          Section "输入输出定义": tensor interface, raw_g = log(alpha) with a
+ *            prefix sum restarted at every chunk, optional initial state,
+ *            GVA head map h_qk = floor(h_v / (Hv / Hq)).
+ *  [SGL]   "sgl-qwen3-5-moe" (rainlin-net), decode node 7
+ *          (gdn_packed_recurrent_qk_norm_gating_state_update): one token,
+ *          decay -> predict -> correct -> read, state held in f32.
+ *
+ * Conventions shared by every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller. The library
+ *    never allocates, frees or synchronises; all work is enqueued on `stream`
+ *    (a cudaStream_t passed as void*, NULL = the legacy default stream).
+ *  - Layouts are contiguous and row-major, token-major:
+ *      q, k   [total_tokens, hq, dk]      io_dtype
+ *      v, out [total_tokens, hv, dv]      io_dtype
+ *      g, beta[total_tokens, hv]          float32 (g is the raw log-decay)
+ *      state  [num_seqs or slots, hv, dk, dv] float32
+ *    Every pointer must be 16-byte aligned.
+ *  - Supported: dk = dv = 128, chunk size 64 (fixed), hv % hq == 0,
+ *    io_dtype GDN_DT_F32 (SIMT f32 arithmetic) or GDN_DT_BF16 (tensor-core
+ *    bf16 operands with f32 accumulation and f32 state). Anything else returns
+ *    GDN_EUNSUPPORTED without launching.
+ *  - Every argument is checked before the first launch; on a non-zero return
+ *    nothing was enqueued and no output was touched.
+ *  - Checks that need device data (cu_seqlens, state_indices) run on the
+ *    device; a failure there is recorded in a device status word (read it with
+ *    gdn_read_device_status) and the affected work is skipped.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_EINVAL = 1,        /* bad pointer, shape, size or alignment */
+    GDN_EUNSUPPORTED = 2,  /* valid but not implemented (dk/dv != 128, flags) */
+    GDN_ECUDA = 3,         /* a CUDA runtime call or launch failed */
+    GDN_ETIMEOUT = 4,      /* a bounded device-side wait gave up */
+    GDN_EDEVICE_INPUT = 5  /* device-side check failed (cu_seqlens, slot index) */
+} gdn_status;
+
+typedef enum gdn_dtype {
+    GDN_DT_F32 = 0,
+    GDN_DT_BF16 = 1
+} gdn_dtype;
+
+/* Problem descriptor.
+ *  Dense prefill  : batch = B, seqlen = T, num_seqs = B, total_tokens = B*T,
+ *                   cu_seqlens = NULL (sequence b = rows [b*T, (b+1)*T)).
+ *  Packed prefill : batch = 1, seqlen = 0, num_seqs = N, total_tokens = rows,
+ *                   cu_seqlens = device int32 [N+1].
+ *  Decode step    : num_seqs = N tokens (one per sequence), total_tokens = N,
+ *                   num_state_slots = rows of the state array.
+ */
+typedef struct gdn_problem {
+    int32_t batch;
+    int32_t seqlen;
+    int32_t num_seqs;
+    int32_t total_tokens;
+    int32_t hq;
+    int32_t hv;
+    int32_t dk;
+    int32_t dv;
+    int32_t io_dtype;         /* gdn_dtype of q, k, v and out */
+    uint32_t flags;           /* reserved, must be 0 */
+    int32_t num_state_slots;  /* decode only */
+} gdn_problem;
+
+/* Workspace bytes gdn_chunk_fwd needs for problem `p` (0 if `p` is invalid).
+ * Sized from an upper bound on the number of 64-token chunks,
+ * total_tokens / 64 + num_seqs, so it does not depend on cu_seqlens values. */
+size_t gdn_chunk_fwd_workspace_size(const gdn_problem *p);
+
+/* Chunk-wise parallel prefill forward ([Lab3] "计算过程描述").
+ *   q, k          [total_tokens, hq, 128]  L2-normalised by the caller
+ *   v             [total_tokens, hv, 128]
+ *   g             [total_tokens, hv] raw per-token log-decay (log alpha);
+ *                 the library does the per-chunk prefix sum
+ *   beta          [total_tokens, hv]
+ *   scale         multiplies every read-out term (1/sqrt(dk) on the pages)
+ *   initial_state [num_seqs, hv, 128, 128] f32, or NULL for zeros
+ *   cu_seqlens    int32 [num_seqs+1] packed offsets, or NULL (dense layout).
+ *                 Must start at 0, be non-decreasing and end at total_tokens
+ *                 (checked on the device). Each sequence starts its own chunk
+ *                 grid; chunks never straddle sequences.
+ *   out           [total_tokens, hv, 128] written for every token
+ *   final_state   [num_seqs, hv, 128, 128] f32, or NULL to skip. A sequence
+ *                 of length 0 copies its initial state (or zeros).
+ *   workspace     device scratch of at least gdn_chunk_fwd_workspace_size(p)
+ *                 bytes, 256-byte aligned; contents need no initialisation
+ *                 and are garbage afterwards. Calls that share a workspace
+ *                 must be ordered on one stream.
+ * Returns GDN_OK once everything is enqueued. */
+int gdn_chunk_fwd(const gdn_problem *p, const void *q, const void *k, const void *v,
+                  const float *g, const float *beta, float scale,
+                  const float *initial_state, const int32_t *cu_seqlens,
+                  void *out, float *final_state,
+                  void *workspace, size_t workspace_bytes, void *stream);
+
+/* Single-token recurrent decode step, state updated in place
+ * ([Lab3] gated delta rule; [SGL] decode node 7 operation order).
+ * For each sequence n < num_seqs and v-head h, with slot s = state_indices[n]
+ * (or n when state_indices is NULL) and alpha = exp(g[n,h]):
+ *   S = alpha * state[s,h];  p = k_n S;  d = beta (v_n - p);
+ *   state[s,h] = S + k_n^T d;  out[n,h] = scale * q_n state[s,h].
+ *   q, k [num_seqs, hq, 128]; v, out [num_seqs, hv, 128]; g, beta [num_seqs, hv]
+ *   state [num_state_slots, hv, 128, 128] f32, read and written in place.
+ *   state_indices int32 [num_seqs] or NULL. A negative index skips the
+ *   sequence (its out rows are not written: a padding slot). An index
+ *   >= num_state_slots is skipped and recorded as GDN_EDEVICE_INPUT.
+ *   Two sequences must not name the same slot (their updates would race). */
+int gdn_recurrent_step(const gdn_problem *p, const void *q, const void *k, const void *v,
+                       const float *g, const float *beta, float scale,
+                       float *state, const int32_t *state_indices,
+                       void *out, void *stream);
+
+/* Synchronises `stream`, returns the device status word (GDN_OK or the first
+ * device-side error recorded since the last clear) and clears it when
+ * `clear` is non-zero. Returns GDN_ECUDA if the CUDA calls themselves fail. */
+int gdn_read_device_status(void *stream, int clear);
+
+/* Static, human-readable name of a gdn_status value. */
+const char *gdn_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int gdn_version(void);
+
+/* ---- measurement hooks (not part of the method; used by benchmarks) ---- */
+
+/* Kernels the library launches, as indices of the gdn_profile_collect arrays. */
+typedef enum gdn_kernel {
+    GDN_K_CHUNK_TABLE = 0,        /* chunk table from cu_seqlens */
+    GDN_K_PREP_SIMT = 1,          /* f32: gate cumsum + KK^T solve + W, U */
+    GDN_K_STATE_SIMT = 2,         /* f32: sequential state pass */
+    GDN_K_OUTPUT_SIMT = 3,        /* f32: chunk output */
+    GDN_K_RECURRENT_STEP = 4,     /* decode step */
+    GDN_K_CHUNK_PREPARE_TC = 5,   /* bf16: gate cumsum + KK^T solve (tensor cores) */
+    GDN_K_STATE_OUTPUT_TC = 6,    /* bf16: W, U, state pass and output (tensor cores) */
+    GDN_K_COUNT = 7
+} gdn_kernel;
+
+/* Turns per-kernel CUDA-event timing on (non-zero) or off for every later
+ * launch (process-wide). Launch counting is always on. */
+int gdn_profile_enable(int enable);
+
+/* Synchronises the recorded events and copies, for the first `count` kernel
+ * ids, the number of launches, the summed event time in ms and the number of
+ * timed launches into the caller's host arrays (any may be NULL). Clears all
+ * counters when `reset` is non-zero. */
+int gdn_profile_collect(long long *launches, double *ms, long long *timed, int count, int reset);
+
+/* Static name of a gdn_kernel id. */
+const char *gdn_kernel_name(int kernel);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

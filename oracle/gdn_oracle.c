@@ -119,6 +119,7 @@ void gdn_oracle_chunked(int64_t N, const int64_t *cu_seqlens, int64_t Hq,
         const int64_t n = pair / Hv, h = pair % Hv, hk = h / G;
         double *S = (double *)calloc((size_t)(dk * dv), sizeof(double));
         double *gc = (double *)malloc((size_t)C * sizeof(double));
+        double *gam = (double *)malloc((size_t)C * sizeof(double));
         double *M = (double *)calloc((size_t)(C * C), sizeof(double));
         double *A = (double *)calloc((size_t)(C * C), sizeof(double));
         double *P = (double *)calloc((size_t)(C * C), sizeof(double));
@@ -158,6 +159,7 @@ void gdn_oracle_chunked(int64_t N, const int64_t *cu_seqlens, int64_t Hq,
                     A[i * C + j] = a;
                 }
             /* U = A diag(beta) V ;  W = A diag(beta gamma) K */
+            for (int64_t j = 0; j < l; ++j) gam[j] = exp(gc[j]);
             for (int64_t i = 0; i < l; ++i) {
                 for (int64_t e = 0; e < dv; ++e) {
                     double acc = 0.0;
@@ -166,7 +168,7 @@ void gdn_oracle_chunked(int64_t N, const int64_t *cu_seqlens, int64_t Hq,
                 }
                 for (int64_t d = 0; d < dk; ++d) {
                     double acc = 0.0;
-                    for (int64_t j = 0; j < l; ++j) acc += A[i * C + j] * BETA(j) * exp(gc[j]) * KROW(j)[d];
+                    for (int64_t j = 0; j < l; ++j) acc += A[i * C + j] * BETA(j) * gam[j] * KROW(j)[d];
                     W[i * dk + d] = acc;
                 }
             }
@@ -203,10 +205,11 @@ void gdn_oracle_chunked(int64_t N, const int64_t *cu_seqlens, int64_t Hq,
             }
             /* S <- gamma_l S + gamma_l K^T Gamma^-1 R */
             const double gl = gc[l - 1];
+            for (int64_t i = 0; i < l; ++i) gam[i] = exp(gl - gc[i]); /* gamma_l / gamma_i */
             for (int64_t d = 0; d < dk; ++d)
                 for (int64_t e = 0; e < dv; ++e) {
                     double acc = 0.0;
-                    for (int64_t i = 0; i < l; ++i) acc += exp(gl - gc[i]) * KROW(i)[d] * R[i * dv + e];
+                    for (int64_t i = 0; i < l; ++i) acc += gam[i] * KROW(i)[d] * R[i * dv + e];
                     Snew[d * dv + e] = exp(gl) * S[d * dv + e] + acc;
                 }
             memcpy(S, Snew, (size_t)(dk * dv) * sizeof(double));
@@ -217,6 +220,6 @@ void gdn_oracle_chunked(int64_t N, const int64_t *cu_seqlens, int64_t Hq,
 #undef BETA
         }
         if (final_state) memcpy(final_state + (n * Hv + h) * dk * dv, S, (size_t)(dk * dv) * sizeof(double));
-        free(Snew); free(R); free(W); free(U); free(P); free(A); free(M); free(gc); free(S);
+        free(Snew); free(R); free(W); free(U); free(P); free(A); free(M); free(gam); free(gc); free(S);
     }
 }

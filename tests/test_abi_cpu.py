@@ -1,0 +1,111 @@
+"""Host-side checks of libgdn.so that need no GPU.
+
+* The library builds, loads and exports every function include/gdn.h declares.
+* Argument checks reject bad problems before any CUDA call (so they can be
+  exercised on a machine without a GPU): wrong head counts, unsupported head
+  dims, bad dtype, flags, misaligned pointers, short workspace.
+* The workspace size query depends only on the problem descriptor.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gated_deltanet_chunked_gb300 import gdn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_symbols():
+    assert set(header_functions()) == set(gdn.SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = gdn.load()
+    for name in header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings():
+    assert gdn.gdn_version() >= 100
+    for s in range(6):
+        assert gdn.gdn_status_string(s).startswith("GDN_")
+    assert "unknown" in gdn.gdn_status_string(99)
+
+
+def problem(**kw):
+    base = dict(batch=1, seqlen=256, num_seqs=1, total_tokens=256, hq=16, hv=32, dk=128, dv=128,
+                io_dtype=gdn.GDN_DT_BF16, flags=0, num_state_slots=0)
+    base.update(kw)
+    return gdn.GdnProblem(**base)
+
+
+FAKE = 1 << 20  # a 16-byte aligned non-null address: never dereferenced by the checks
+
+
+def call_fwd(p, ws_bytes=1 << 40, ptr=FAKE, ws=FAKE << 8, cu=None):
+    lib = gdn.load()
+    P = ctypes.c_void_p
+    return lib.gdn_chunk_fwd(ctypes.byref(p), P(ptr), P(ptr), P(ptr), P(ptr), P(ptr), ctypes.c_float(0.1), None,
+                             None if cu is None else P(cu), P(ptr), None, P(ws), ctypes.c_size_t(ws_bytes), None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(hv=33), gdn.GDN_EINVAL),           # hv % hq != 0
+    (dict(hq=0), gdn.GDN_EINVAL),
+    (dict(dk=64, dv=64), gdn.GDN_EUNSUPPORTED),
+    (dict(dk=0), gdn.GDN_EINVAL),
+    (dict(io_dtype=7), gdn.GDN_EINVAL),
+    (dict(flags=1), gdn.GDN_EUNSUPPORTED),
+    (dict(total_tokens=255), gdn.GDN_EINVAL),  # dense: B*T != total
+    (dict(num_seqs=2), gdn.GDN_EINVAL),        # dense: num_seqs != batch
+    (dict(num_seqs=0), gdn.GDN_EINVAL),
+])
+def test_chunk_fwd_rejects_bad_problems(kw, code):
+    assert call_fwd(problem(**kw)) == code
+
+
+def test_chunk_fwd_rejects_bad_pointers_and_workspace():
+    p = problem()
+    need = gdn.gdn_chunk_fwd_workspace_size(p)
+    assert need > 0
+    assert call_fwd(p, ptr=FAKE + 4) == gdn.GDN_EINVAL           # misaligned tensor
+    assert call_fwd(p, ptr=0) == gdn.GDN_EINVAL                  # NULL tensor
+    assert call_fwd(p, ws_bytes=need - 1) == gdn.GDN_EINVAL      # short workspace
+    assert call_fwd(p, ws=(FAKE << 8) + 16) == gdn.GDN_EINVAL    # workspace not 256-aligned
+    assert call_fwd(p, cu=FAKE + 8) == gdn.GDN_EINVAL            # misaligned cu_seqlens
+
+
+def test_workspace_size_query():
+    p = problem()
+    a = gdn.gdn_chunk_fwd_workspace_size(p)
+    b = gdn.gdn_chunk_fwd_workspace_size(problem(batch=1, seqlen=0, num_seqs=1))  # packed descriptor
+    assert a == b > 0
+    assert gdn.gdn_chunk_fwd_workspace_size(problem(hv=33)) == 0
+    # grows with tokens and with sequences (chunk upper bound T/64 + N)
+    assert gdn.gdn_chunk_fwd_workspace_size(problem(seqlen=0, total_tokens=4096)) > a
+    assert (gdn.gdn_chunk_fwd_workspace_size(problem(seqlen=0, num_seqs=8)) >
+            gdn.gdn_chunk_fwd_workspace_size(problem(seqlen=0, num_seqs=1)))
+
+
+def test_recurrent_step_rejects_bad_problems():
+    lib = gdn.load()
+    P = ctypes.c_void_p
+
+    def step(p, idx=None, ptr=FAKE):
+        return lib.gdn_recurrent_step(ctypes.byref(p), P(ptr), P(ptr), P(ptr), P(ptr), P(ptr), ctypes.c_float(1.0),
+                                      P(ptr), None if idx is None else P(idx), P(ptr), None)
+
+    ok = dict(batch=4, seqlen=1, num_seqs=4, total_tokens=4, num_state_slots=4)
+    assert step(problem(**{**ok, "num_state_slots": 3})) == gdn.GDN_EINVAL  # identity map needs N slots
+    assert step(problem(**{**ok, "total_tokens": 5})) == gdn.GDN_EINVAL
+    assert step(problem(**{**ok, "dk": 96})) == gdn.GDN_EUNSUPPORTED
+    assert step(problem(**ok), ptr=FAKE + 2) == gdn.GDN_EINVAL
+    assert step(problem(**ok), idx=FAKE + 4) == gdn.GDN_EINVAL

@@ -1,0 +1,131 @@
+"""Parity of gdn_chunk_fwd (CUDA, through the C ABI) with the CPU oracle.
+
+Element-by-element comparison on seeded inputs:
+  * f32 path: max|x - ref| / max|ref| <= 1e-4 on o and on the final state;
+  * bf16 path: normwise relative error <= 2e-2 on o and on the final state.
+Small cases span several chunks and ragged tails (lengths 1, 63, 64, 65, ...),
+empty sequences, GVA groups 1/2/4 and present/absent initial states. The
+full-size workloads are checked in the launch configuration the benchmark
+times: T=4096 in full, varlen and T=65536 on sampled q/k head groups that the
+oracle computes independently.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gated_deltanet_chunked_gb300 import gdn, workloads as W
+from parity_util import check, head_slice, oracle_prefill, run_gpu_prefill
+
+pytestmark = pytest.mark.gpu
+
+
+def test_tiny_f32_workload(cuda):
+    inp = W.make_prefill(W.WORKLOADS["tiny_f32_T200"])
+    o, S = run_gpu_prefill(inp, cuda, packed=False)
+    o_ref, S_ref = oracle_prefill(inp)
+    check(o, o_ref, torch.float32, "o")
+    check(S, S_ref, torch.float32, "final_state")
+
+
+CASES = [
+    ([1], 1, 1, True),
+    ([64], 1, 2, False),
+    ([65], 2, 4, True),
+    ([63, 1, 0, 64, 130], 1, 2, True),
+    ([200], 2, 2, True),
+    ([0, 0], 1, 1, True),
+    ([129, 7], 2, 8, False),
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("lengths,hq,hv,with_s0", CASES)
+def test_ragged_cases(cuda, dtype, lengths, hq, hv, with_s0):
+    inp = W.make_custom_prefill(100 + sum(lengths) + hv, lengths, hq, hv, dtype, s0_sigma=0.1 if with_s0 else None)
+    o, S = run_gpu_prefill(inp, cuda)
+    o_ref, S_ref = oracle_prefill(inp)
+    if inp["total_tokens"]:
+        check(o, o_ref, dtype, "o")
+    check(S, S_ref, dtype, "final_state")
+    if not with_s0:  # empty sequences must report a zero state
+        for n, L in enumerate(lengths):
+            if L == 0:
+                assert torch.count_nonzero(S[n]) == 0
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_dense_layout_equals_packed(cuda, dtype):
+    inp = W.make_custom_prefill(7, [100, 100], 2, 4, dtype, s0_sigma=0.05)
+    o_p, S_p = run_gpu_prefill(inp, cuda)
+    d = {k: (v.to(cuda) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    rs = lambda x: x.reshape(2, 100, *x.shape[1:])
+    o_d, S_d = gdn.gdn_chunk_fwd(rs(d["q"]), rs(d["k"]), rs(d["v"]), rs(d["g"]), rs(d["beta"]), d["scale"],
+                                 initial_state=d["initial_state"])
+    torch.cuda.synchronize()
+    assert torch.equal(o_d.reshape(o_p.shape), o_p)
+    assert torch.equal(S_d, S_p)
+
+
+def test_bit_reproducible_and_permutation_invariant(cuda):
+    lengths = [70, 200, 1, 129]
+    inp = W.make_custom_prefill(11, lengths, 2, 4, torch.bfloat16, s0_sigma=0.05)
+    o1, S1 = run_gpu_prefill(inp, cuda)
+    o2, S2 = run_gpu_prefill(inp, cuda)
+    assert torch.equal(o1, o2) and torch.equal(S1, S2)
+    cu = inp["cu_seqlens"].tolist()
+    perm = [3, 1, 0, 2]
+    seg = lambda x: [x[cu[i]:cu[i + 1]] for i in range(len(lengths))]
+    cat = lambda x: torch.cat([seg(x)[p] for p in perm])
+    inp2 = dict(inp)
+    for key in ("q", "k", "v", "g", "beta"):
+        inp2[key] = cat(inp[key])
+    inp2["initial_state"] = inp["initial_state"][perm]
+    inp2["cu_seqlens"] = torch.tensor(np.concatenate([[0], np.cumsum([lengths[p] for p in perm])]),
+                                      dtype=torch.int32)
+    o3, S3 = run_gpu_prefill(inp2, cuda)
+    assert torch.equal(o3, cat(o1.cpu()).to(cuda))
+    assert torch.equal(S3, S1[perm])
+
+
+def test_no_final_state(cuda):
+    inp = W.make_custom_prefill(12, [90], 1, 2, torch.bfloat16)
+    o, S = run_gpu_prefill(inp, cuda, output_final_state=False)
+    assert S is None
+    check(o, oracle_prefill(inp)[0], torch.bfloat16, "o")
+
+
+def test_bad_cu_seqlens_sets_device_status(cuda):
+    inp = W.make_custom_prefill(13, [64, 64], 1, 1, torch.float32)
+    d = {k: (v.to(cuda) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    gdn.gdn_read_device_status(clear=True)
+    out = torch.full_like(d["v"], 7.0)
+    fin = torch.full((2, 1, 128, 128), 7.0, device=cuda)
+    bad = torch.tensor([0, 100, 90], dtype=torch.int32, device=cuda)  # decreasing and short of total
+    gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], cu_seqlens=bad, out=out,
+                      final_state=fin)
+    assert gdn.gdn_read_device_status(clear=True) == gdn.GDN_EDEVICE_INPUT
+    assert torch.all(out == 7.0) and torch.all(fin == 7.0)  # nothing written
+    assert gdn.gdn_read_device_status() == gdn.GDN_OK
+
+
+def test_prefill_T4096_full(cuda):
+    w = W.WORKLOADS["prefill_T4096_hq16_hv32"]
+    inp = W.make_prefill(w)
+    o, S = run_gpu_prefill(inp, cuda)
+    o_ref, S_ref = oracle_prefill(inp)
+    check(o, o_ref, torch.bfloat16, "o")
+    check(S, S_ref, torch.bfloat16, "final_state")
+
+
+@pytest.mark.parametrize("name,heads", [("varlen_8seq_hq16_hv32", [0, 9]), ("long_T65536_hq16_hv32", [5])])
+def test_large_workloads_sampled_heads(cuda, name, heads):
+    w = W.WORKLOADS[name]
+    inp = W.make_prefill(w)
+    o, S = run_gpu_prefill(inp, cuda)
+    G = w.hv // w.hq
+    for hk in heads:
+        sub = head_slice(inp, hk, G)
+        o_ref, S_ref = oracle_prefill(sub)
+        hv = slice(hk * G, (hk + 1) * G)
+        check(o[:, hv], o_ref, torch.bfloat16, f"o[{name}, heads {hv}]")
+        check(S[:, hv], S_ref, torch.bfloat16, f"final_state[{name}, heads {hv}]")
