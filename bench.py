@@ -1,0 +1,490 @@
+#!/usr/bin/env python
+"""Benchmark of the Gated DeltaNet forward on one node of GB300 GPUs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one gdn_chunk_fwd call over the single-sequence prefill workload
+(B=1, T=4096, Hq=16, Hv=32, d=128, bf16 q/k/v, f32 g/beta, zero initial
+state, f32 final state), inputs resident in HBM. Between timed steps the L2 is
+flushed by writing a 512 MiB buffer (the inputs, 104 MB, would fit in the
+126 MB L2). Prints ONE JSON line (rank 0). The decode step (256 sequences x 32
+v-heads, f32 state read and written in place) is measured in the same run and
+reported under "decode".
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs its own replica of the
+workload (weak scaling: the GDN core shards over sequences and heads with no
+exchange); a barrier brackets the timed region and the slowest rank's time is
+taken.
+
+--impl reference times the CPU oracle (plain C, float64, OpenMP) on the same
+workload: each step runs a bounded sample (a quarter of the q/k head groups)
+and the rate is scaled to the whole workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from gated_deltanet_chunked_gb300 import workloads as W  # noqa: E402
+
+METRIC = "GDN prefill tokens/s (T=4096,Hv=32,d=128) & % roofline; decode state GB/s"
+PREFILL = W.WORKLOADS["prefill_T4096_hq16_hv32"]
+DECODE = W.WORKLOADS["decode_N256_hq16_hv32"]
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20
+
+
+# --------------------------------------------------------------------------
+# algorithmic byte / flop model (per token, per sequence, per chunk)
+# --------------------------------------------------------------------------
+def prefill_bytes(T, N, hq, hv, io_bytes=2, s0=False, final=True, d=128):
+    per_tok = hq * d * io_bytes * 2 + hv * d * io_bytes * 2 + hv * 8  # q,k + v,o + g,beta
+    per_seq = hv * d * d * 4 * (int(s0) + int(final))
+    return T * per_tok + N * per_seq
+
+
+def prefill_flops(n_chunk_heads, hv, hq, C=64, d=128):
+    G = hv // hq
+    per = 6 * C * d * d + C * C * (d + d) + C * C * d + 2 * C * C * d / G
+    return n_chunk_heads * per
+
+
+def kernel_bytes(name, T, N, hq, hv, io_bytes=2, s0=False, final=True, d=128):
+    """Compulsory HBM bytes of one launch of a kernel (its share of the path's
+    inputs and outputs; intermediates kept in workspace are not counted)."""
+    qk = T * hq * d * io_bytes
+    vv = T * hv * d * io_bytes
+    gb = T * hv * 8
+    st = N * hv * d * d * 4 * (int(s0) + int(final))
+    return {
+        "chunk_table": 4 * (N + 1),
+        "prep_simt": qk + vv + gb,
+        "state_simt": qk + st,
+        "output_simt": 2 * qk + vv,
+        "chunk_prepare_tc": qk + gb,
+        "chunk_state_output_tc": 2 * qk + 2 * vv + gb + st,
+    }.get(name)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "gated_deltanet_chunked_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("source_hash") != source_hash():
+        return None
+    k = d.get("kernels", {}).get(kernel)
+    return None if k is None else k.get("dram_bytes_per_launch")
+
+
+# --------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index, period_ms=50):
+        self.gpu_index, self.period_ms = gpu_index, period_ms
+        self.samples, self.proc, self.thread = [], None, None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", str(self.period_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        win = [s for t, s in self.samples if t0 - 0.06 <= t <= t1 + 0.06]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        sm = []
+        for s in win:
+            try:
+                sm.append(float(s[1]))
+            except ValueError:
+                pass
+            for i, n in enumerate(names):
+                if len(s) > 5 + i and s[5 + i].lower() == "active":
+                    reasons.add(n)
+        try:
+            smax = float(win[-1][2])
+        except ValueError:
+            smax = None
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(win), "power_w_max": max((float(s[3]) for s in win if _isnum(s[3])), default=None)}
+
+
+def _isnum(x):
+    try:
+        float(x)
+        return True
+    except ValueError:
+        return False
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (timing only; the data path has no collective)
+# --------------------------------------------------------------------------
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend, init_method="env://")
+    return world, rank, local
+
+
+def barrier(world, dev=None):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x, world, dev):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+def run_ours(args, world, rank, local):
+    from gated_deltanet_chunked_gb300 import gdn
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the CUDA path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    gdn.load()
+    peaks, peak_src = load_peaks()
+
+    w = PREFILL
+    host = W.make_prefill(w)
+    T, N = host["total_tokens"], host["num_seqs"]
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+    out = torch.empty_like(d["v"])
+    fin = torch.empty((N, w.hv, 128, 128), dtype=torch.float32, device=dev)
+    prob = gdn.prefill_problem(d["q"], d["v"], N, packed=True)
+    ws = torch.empty(gdn.gdn_chunk_fwd_workspace_size(prob), dtype=torch.uint8, device=dev)
+    cu = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], initial_state=None, cu_seqlens=cu,
+                          out=out, final_state=fin, workspace=ws)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert gdn.gdn_read_device_status() == gdn.GDN_OK
+
+    clocks = ClockSampler(local).start()
+    time.sleep(0.3)
+    gdn.gdn_profile_collect(reset=True)
+    gdn.gdn_profile_enable(True)
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        ev0[i].record()
+        step()
+        ev1[i].record()
+    torch.cuda.synchronize()
+    t_end = time.time()
+    barrier(world)
+    gdn.gdn_profile_enable(False)
+    prof = gdn.gdn_profile_collect(reset=True)
+    step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    ms_local = sum(step_ms) / len(step_ms)
+    ms = max_over_ranks(ms_local, world, dev)
+    value = world * T / (ms * 1e-3)
+
+    # dominant kernel of the timed region
+    kernels = {k: {"launches": n, "ms_total": t, "ms_per_launch": t / max(nt, 1)} for k, (n, t, nt) in prof.items()}
+    dom = max(kernels, key=lambda k: kernels[k]["ms_total"])
+    dom_bytes = kernel_bytes(dom, T, N, w.hq, w.hv)
+    dom_ms = kernels[dom]["ms_per_launch"]
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    path_bytes = prefill_bytes(T, N, w.hq, w.hv)
+    n_chunk_heads = math.ceil(T / 64) * w.hv
+    path_flops = prefill_flops(n_chunk_heads, w.hv, w.hq)
+    roofline = {
+        "kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+        "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(dom),
+        "peak_source": f"{peak_src} (hbm_gbs, burst copy)",
+        "algorithmic_bytes_per_launch": dom_bytes,
+        "path": {
+            "bytes": path_bytes, "flops": path_flops,
+            "t_bytes_us": path_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6,
+            "t_flops_us": path_flops / (peaks["bf16_tflops"] * 1e12) * 1e6,
+            "frac_of_roofline": max(path_bytes / (peaks["hbm_gbs"] * 1e9),
+                                    path_flops / (peaks["bf16_tflops"] * 1e12)) / (ms * 1e-3),
+        },
+    }
+    gpu_launches = sum(v["launches"] for v in kernels.values())
+
+    # end to end through the public API: pinned host inputs -> device -> host
+    pin = {k: host[k].pin_memory() for k in ("q", "k", "v", "g", "beta")}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    fin_h = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+    dev_in = {k: torch.empty_like(d[k]) for k in pin}
+    bi = sum(t.numel() * t.element_size() for t in pin.values())
+    bo = out_h.numel() * out_h.element_size() + fin_h.numel() * fin_h.element_size()
+
+    def e2e_step():
+        for k in pin:
+            dev_in[k].copy_(pin[k], non_blocking=True)
+        gdn.gdn_chunk_fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"], d["scale"],
+                          cu_seqlens=cu, out=out, final_state=fin, workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+        fin_h.copy_(fin, non_blocking=True)
+
+    for _ in range(max(2, args.warmup)):
+        e2e_step()
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        e0[i].record()
+        e2e_step()
+        e1[i].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(e0, e1)) / args.steps, world, dev)
+    e2e = {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": bi,
+           "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms}
+
+    decode = None if args.no_decode else run_decode(args, dev, world, peaks, peak_src)
+    clocks.stop()
+    clk = clocks.summary(t_start, t_end)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(host, w, fraction=0.5)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": 1, "T": T, "hq": w.hq, "hv": w.hv, "dk": 128, "dv": 128,
+                   "chunk": 64, "initial_state": "zero", "final_state": "f32",
+                   "l2": "flushed between timed steps (512 MiB write)", "parallelism": f"replicas x{world}"},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": gpu_launches,
+        "kernels": kernels, "decode": decode,
+        "step_ms": {"median": statistics.median(step_ms), "p10": sorted(step_ms)[len(step_ms) // 10],
+                    "p90": sorted(step_ms)[(9 * len(step_ms)) // 10]},
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_decode(args, dev, world, peaks, peak_src):
+    from gated_deltanet_chunked_gb300 import gdn
+
+    w = DECODE
+    state = W.make_decode_state(w).to(dev)
+    sets = []
+    for s in range(4):
+        inp = W.make_decode_step(w, s)
+        sets.append({k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()})
+    out = torch.empty_like(sets[0]["v"])
+
+    def step(i):
+        x = sets[i % len(sets)]
+        gdn.gdn_recurrent_step(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], state, out=out)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    steps = max(10, min(args.steps, 100))
+    gdn.gdn_profile_collect(reset=True)
+    gdn.gdn_profile_enable(True)
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        e0[i].record()
+        step(i)
+        e1[i].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    gdn.gdn_profile_enable(False)
+    prof = gdn.gdn_profile_collect(reset=True)
+    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(e0, e1)) / steps, world, dev)
+    n_pairs = w.num_seqs * w.hv
+    state_bytes = 2 * n_pairs * 128 * 128 * 4
+    io_bytes = w.num_seqs * (w.hq * 128 * 2 * 2 + w.hv * 128 * 2 * 2 + w.hv * 8)
+    total = state_bytes + io_bytes
+    n, kms, nt = prof.get("recurrent_step", (0, 0.0, 0))
+    k_ms = kms / max(nt, 1)
+    return {
+        "workload": w.name, "steps": steps, "ms_per_step": ms, "value": world * total / (ms * 1e-3) / 1e9,
+        "unit": "GB/s", "state_bytes_per_step": state_bytes, "bytes_per_step": total,
+        "roofline": {"kernel": "recurrent_step", "bound": "hbm", "achieved": total / (k_ms * 1e-3) / 1e9,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": total / (k_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "traffic": ncu_traffic("recurrent_step"),
+                     "peak_source": f"{peak_src} (hbm_gbs, burst copy)"},
+        "l2": "state (537 MB) larger than L2; no flush",
+    }
+
+
+def cpu_baseline(host, w, fraction):
+    """Times the CPU oracle (chunk form) on a bounded sample of the workload:
+    the first `fraction` of the q/k head groups, all tokens."""
+    import oracle
+
+    G = w.hv // w.hq
+    nk = max(1, int(w.hq * fraction))
+    q, k = host["q"][:, :nk], host["k"][:, :nk]
+    v, g, beta = host["v"][:, :nk * G], host["g"][:, :nk * G], host["beta"][:, :nk * G]
+    T = host["total_tokens"]
+    oracle.build()
+    t = time.perf_counter()
+    oracle.chunked(q, k, v, g, beta, host["scale"], None, [0, T])
+    dt = time.perf_counter() - t
+    frac = nk / w.hq
+    return {"value": T * frac / dt, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"chunk-form oracle (f64) over all {T} tokens of {nk}/{w.hq} q/k head groups "
+                      f"({nk * G}/{w.hv} v-heads), one pass, {dt:.2f} s; rate scaled by the head fraction"}
+
+
+# --------------------------------------------------------------------------
+# reference arm: the CPU oracle as it stands
+# --------------------------------------------------------------------------
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+
+    w = PREFILL
+    host = W.make_prefill(w)
+    T = host["total_tokens"]
+    G = w.hv // w.hq
+    nk = max(1, w.hq // 2)
+    q, k = host["q"][:, :nk], host["k"][:, :nk]
+    v, g, beta = host["v"][:, :nk * G], host["g"][:, :nk * G], host["beta"][:, :nk * G]
+    oracle.build()
+    for _ in range(args.warmup):
+        oracle.chunked(q, k, v, g, beta, host["scale"], None, [0, T])
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle.chunked(q, k, v, g, beta, host["scale"], None, [0, T])
+        times.append(time.perf_counter() - t)
+    sec = sum(times) / len(times) * (w.hq / nk)  # seconds for the whole workload
+    value = T / sec
+    sample = (f"chunk-form oracle (f64, OpenMP) per step over all {T} tokens of {nk}/{w.hq} q/k head groups; "
+              f"rate scaled to all {w.hv} v-heads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": 1, "T": T, "hq": w.hq, "hv": w.hv, "dk": 128, "dv": 128, "chunk": 64},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.gpus != world and world > 1:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
