@@ -18,11 +18,13 @@ import torch
 
 from . import build as _build
 
-GDN_OK, GDN_EINVAL, GDN_EUNSUPPORTED, GDN_ECUDA, GDN_ETIMEOUT, GDN_EDEVICE_INPUT = range(6)
+GDN_OK, GDN_EINVAL, GDN_EUNSUPPORTED, GDN_ECUDA, GDN_ETIMEOUT, GDN_EDEVICE_INPUT, GDN_ETOOBIG = range(7)
+GDN_NOALLOC_SCRATCH_BYTES = 32 << 20
 GDN_DT_F32, GDN_DT_BF16 = 0, 1
 
 SYMBOLS = ("gdn_chunk_fwd", "gdn_chunk_fwd_workspace_size", "gdn_recurrent_step", "gdn_read_device_status",
-           "gdn_status_string", "gdn_version", "gdn_profile_enable", "gdn_profile_collect", "gdn_kernel_name")
+           "gdn_status_string", "gdn_version", "gdn_profile_enable", "gdn_profile_collect", "gdn_kernel_name",
+           "gdn_chunk_fwd_noalloc")
 GDN_K_COUNT = 7
 
 
@@ -68,6 +70,9 @@ def load(path: Optional[str] = None):
             lib.gdn_profile_enable.restype = ctypes.c_int
             lib.gdn_profile_collect.argtypes = [_vp, _vp, _vp, ctypes.c_int, ctypes.c_int]
             lib.gdn_profile_collect.restype = ctypes.c_int
+            lib.gdn_chunk_fwd_noalloc.argtypes = [P, _vp, _vp, _vp, _fp, _fp, ctypes.c_float, _fp, _ip, _vp, _fp,
+                                                  _vp]
+            lib.gdn_chunk_fwd_noalloc.restype = ctypes.c_int
             lib.gdn_kernel_name.argtypes = [ctypes.c_int]
             lib.gdn_kernel_name.restype = ctypes.c_char_p
             _lib = lib
@@ -147,6 +152,23 @@ def gdn_chunk_fwd(q, k, v, g, beta, scale, initial_state=None, cu_seqlens=None, 
                               _stream(stream))
     if st != GDN_OK:
         raise GdnError(st, "gdn_chunk_fwd")
+    return out, final_state
+
+
+def gdn_chunk_fwd_noalloc(q, k, v, g, beta, scale, out, final_state=None, initial_state=None, cu_seqlens=None,
+                          stream=None):
+    """gdn_chunk_fwd without a workspace, for callers that cannot allocate:
+    the library uses its fixed device scratch array (GDN_NOALLOC_SCRATCH_BYTES)
+    and allocates nothing. ``out`` (and ``final_state`` if wanted) must be
+    supplied. Raises GdnError(GDN_ETOOBIG) for problems above that size."""
+    packed = cu_seqlens is not None
+    num_seqs = cu_seqlens.numel() - 1 if packed else q.shape[0]
+    prob = prefill_problem(q, v, num_seqs, packed)
+    st = load().gdn_chunk_fwd_noalloc(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                      ctypes.c_float(scale), _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
+                                      _ptr(final_state), _stream(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_chunk_fwd_noalloc")
     return out, final_state
 
 

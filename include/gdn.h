@@ -56,7 +56,8 @@ typedef enum gdn_status {
     GDN_EUNSUPPORTED = 2,  /* valid but not implemented (dk/dv != 128, flags) */
     GDN_ECUDA = 3,         /* a CUDA runtime call or launch failed */
     GDN_ETIMEOUT = 4,      /* a bounded device-side wait gave up */
-    GDN_EDEVICE_INPUT = 5  /* device-side check failed (cu_seqlens, slot index) */
+    GDN_EDEVICE_INPUT = 5, /* device-side check failed (cu_seqlens, slot index) */
+    GDN_ETOOBIG = 6        /* problem exceeds the fixed scratch of gdn_chunk_fwd_noalloc */
 } gdn_status;
 
 typedef enum gdn_dtype {
@@ -116,6 +117,32 @@ int gdn_chunk_fwd(const gdn_problem *p, const void *q, const void *k, const void
                   const float *initial_state, const int32_t *cu_seqlens,
                   void *out, float *final_state,
                   void *workspace, size_t workspace_bytes, void *stream);
+
+/* Bytes of the static device scratch array behind gdn_chunk_fwd_noalloc. */
+#define GDN_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* gdn_chunk_fwd for callers that cannot allocate device memory.
+ * The method itself has no counterpart of this entry point on the pages; it
+ * exists for callers that are not allowed to call cudaMalloc (for example
+ * code running inside a memory allocator's own hooks, a host callback, or a
+ * runtime that fixes its memory footprint after start-up) and so cannot hand
+ * over a workspace. Same arguments and results as gdn_chunk_fwd, minus the
+ * workspace: the scratch lives in one file-scope device array of
+ * GDN_NOALLOC_SCRATCH_BYTES (32 MiB) that every GPU loading the library holds
+ * until the process exits. No call allocates or frees anything.
+ *  - Returns GDN_ETOOBIG, without launching, when
+ *    gdn_chunk_fwd_workspace_size(p) > GDN_NOALLOC_SCRATCH_BYTES.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - All calls share the one array and it keeps the last call's contents;
+ *    nothing in it needs to start at zero. Calls whose work overlaps on the
+ *    GPU (different streams, different host threads without ordering) race
+ *    on it: order them on one stream. */
+int gdn_chunk_fwd_noalloc(const gdn_problem *p, const void *q, const void *k, const void *v,
+                          const float *g, const float *beta, float scale,
+                          const float *initial_state, const int32_t *cu_seqlens,
+                          void *out, float *final_state, void *stream);
 
 /* Single-token recurrent decode step, state updated in place
  * ([Lab3] gated delta rule; [SGL] decode node 7 operation order).

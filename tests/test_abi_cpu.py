@@ -35,7 +35,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_version_and_status_strings():
     assert gdn.gdn_version() >= 100
-    for s in range(6):
+    for s in range(7):
         assert gdn.gdn_status_string(s).startswith("GDN_")
     assert "unknown" in gdn.gdn_status_string(99)
 
