@@ -73,7 +73,7 @@ WsLayout ws_layout(const gdn_problem *p) {
     l.seq_off = 256;
     l.chunk_off = l.seq_off + align256(sizeof(SeqInfo) * size_t(p->num_seqs));
     l.data_off = l.chunk_off + align256(sizeof(ChunkInfo) * size_t(mc));
-    l.data_bytes = prefill_simt_workspace(mc, p->hv);
+    l.data_bytes = p->io_dtype == GDN_DT_BF16 ? prefill_tc_workspace(mc, p->hv) : prefill_simt_workspace(mc, p->hv);
     l.total = l.data_off + l.data_bytes;
     return l;
 }
@@ -145,7 +145,8 @@ int gdn_chunk_fwd(const gdn_problem *p, const void *q, const void *k, const void
     a.status = status;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if ((st = cuda_status(launch_chunk_table(a, s)))) return st;
-    return cuda_status(launch_prefill_simt(a, p->io_dtype == GDN_DT_BF16, ws + L.data_off, s));
+    if (p->io_dtype == GDN_DT_BF16) return cuda_status(launch_prefill_tc(a, ws + L.data_off, s));
+    return cuda_status(launch_prefill_simt(a, ws + L.data_off, s));
 }
 
 int gdn_recurrent_step(const gdn_problem *p, const void *q, const void *k, const void *v, const float *g,

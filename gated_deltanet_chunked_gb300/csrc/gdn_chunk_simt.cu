@@ -281,8 +281,8 @@ size_t prefill_simt_workspace(int max_chunks, int hv) {
            2 * align256(units * kChunk * kHeadDim * 4) + align256(units * kHeadDim * kHeadDim * 4);
 }
 
-cudaError_t launch_prefill_simt(const PrefillArgs &a, bool bf16, void *ws_data, cudaStream_t s) {
-    return bf16 ? launch_all<__nv_bfloat16>(a, ws_data, s) : launch_all<float>(a, ws_data, s);
+cudaError_t launch_prefill_simt(const PrefillArgs &a, void *ws_data, cudaStream_t s) {
+    return launch_all<float>(a, ws_data, s);
 }
 
 }  // namespace gdn

@@ -83,8 +83,10 @@ class LaunchScope {
 
 // Host-side launchers implemented in the kernel translation units.
 cudaError_t launch_chunk_table(const PrefillArgs &a, cudaStream_t s);
-cudaError_t launch_prefill_simt(const PrefillArgs &a, bool bf16, void *ws_data, cudaStream_t s);
+cudaError_t launch_prefill_simt(const PrefillArgs &a, void *ws_data, cudaStream_t s);
 size_t prefill_simt_workspace(int max_chunks, int hv);
+cudaError_t launch_prefill_tc(const PrefillArgs &a, void *ws_data, cudaStream_t s);
+size_t prefill_tc_workspace(int max_chunks, int hv);
 cudaError_t launch_recurrent_step(const gdn_problem &p, const void *q, const void *k, const void *v,
                                   const float *g, const float *beta, float scale, float *state,
                                   const int32_t *state_indices, void *out, int *status, cudaStream_t s);
