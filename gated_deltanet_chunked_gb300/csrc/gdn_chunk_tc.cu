@@ -1,38 +1,42 @@
 // Chunk-form prefill on the tensor cores (the GDN_DT_BF16 path), sm_103a.
 //
-// The Lab3 GDN Prefill page, section "计算过程描述", split into two kernels:
+// Method (Lab3 GDN Prefill page, section "计算过程描述"), per chunk c of valid
+// length l_c, with gc the per-chunk prefix sum of the raw gates:
+//   A_c = (I + StrictLower(B Gamma K K^T Gamma^-1))^-1,  U_c = A_c B V,
+//   W_c = A_c B Gamma K,  V'_c = U_c - W_c S_c,
+//   S_{c+1} = gamma_c S_c + K_c^T diag(d_c) V'_c,   d_{c,i} = exp(gc_{l-1} - gc_i)
+//   O_c = scale [Gamma Q_c S_c + P_c V'_c],  P_c = Lower(Q K^T) * exp(gc_r - gc_i)
 //
-// k_chunk_prepare_tc  (grid: chunk x q/k head; chunk-parallel)
-//   chunk_gate_cumsum: gc_r = sum_{j<=r} g_j, restarted per chunk
-//   chunk_kkt_solve:   K K^T on tcgen05 (shared by the G v-heads of the q/k
-//                      head), M_ij = beta_i exp(gc_i - gc_j) (K K^T)_ij for
-//                      j < i < l, A = (I + M)^-1 by forward substitution in
-//                      f32 (thread j owns column j in registers)
-//   writes A diag(beta) as a bf16 64x64 tile already in the 128B-swizzled
-//   K-major layout the MMA reads, plus gc and beta of the chunk.
+// A tcgen05 MMA round trip (issue, completion, wake-up) costs about 900 SM
+// cycles on this part whatever its size, so a serial walk with two dependent
+// products per chunk (W S, then K^T V') is latency-bound. Substituting the
+// state update into the next chunk's V' removes one of them:
+//   V'_{c+1} = U_{c+1} - (gamma_c W_{c+1}) S_c - G_c V'_c,
+//   G_c = W_{c+1} K_c^T diag(d_c)                    (chunk-parallel)
+// so (S_{c+1}, V'_{c+1}, O_c) all follow from (S_c, V'_c) in ONE batch of
+// MMAs. Stacking the two 64-row products that share a right operand gives
+// M = 128 MMAs (an M = 64 MMA runs at half the rate):
+//   D1 = [A_c+1 B ; 0] V_{c+1} + [-gamma_c W_{c+1} ; Gamma_c Q_c] S_c
+//        + [-G_c ; P_c] V'_c         rows 0..63 = V'_{c+1}, rows 64..127 = O_c/scale
+//   D2 = K_c^T (diag(d_c) V'_c)      S_{c+1} = gamma_c S_c + D2
+// The walk starts at a virtual step c = -1 with S_-1 = S0, V'_-1 = 0,
+// gamma_-1 = 1 and G_-1 = 0, which yields V'_0 = U_0 - W_0 S0.
 //
-// k_chunk_state_output_tc  (grid: 64-column tile of dv x v-head x sequence)
-//   walks the chunks of its sequence in order, with the f32 state tile
-//   S [128 x 64] held in registers (thread t owns row t):
-//   chunk_recompute_w_u: W = (A diag(beta) Gamma) K, U = (A diag(beta)) V
-//   chunk_state_h:       V' = U - W S, S <- gamma_l S + K^T (diag(gamma_l /
-//                        gamma_i) V')
-//   chunk_output_o:      O = scale [Gamma (Q S) + P V'],
-//                        P = Lower(Q K^T) masked and scaled by exp(gc_r - gc_i)
-//   Seven tcgen05 MMAs per chunk (bf16 operands in shared memory, f32
-//   accumulators in tensor memory); q/k/v tiles arrive by TMA, A and the
-//   gates by bulk copy, double-buffered one chunk ahead.
+// k_chunk_prepare_tc (grid: chunk x q/k head, all SMs): gate prefix sums,
+//   [K;Q] K^T in one M=128 MMA, the masked gated M and its unit-lower-
+//   triangular inverse by blocked (16x16) forward substitution in f32, then
+//   W_c and G_{c-1} on the tensor cores. Writes, per (chunk, v-head), bf16
+//   tiles already in the 128B-swizzled K-major layout the state kernel's
+//   MMAs read: A B, -gamma_{c-1} W_c, -G_{c-1}, P_c; and f32 gc, beta.
+// k_chunk_state_output_tc (grid: 64-wide dv tile x v-head x sequence): the
+//   serial walk. One producer warp (TMA for q/k/v tiles, bulk copies for the
+//   prepared tiles, two step buffers), one MMA warp, four math warps holding
+//   the f32 state tile S[128 x 64] in registers (thread t = row t).
 //
-// Shared-memory operand layouts (all 128-byte swizzled, 1024-byte aligned):
-//   [rows][64 bf16] tiles; a 128-wide tile is two 64-wide halves 8 KiB apart
-//   (64 rows) so one buffer serves as a K-major operand (rows = M/N) and as
-//   an MN-major operand (rows = K) of different MMAs.
-// Tensor-memory layout of an M=64 accumulator: row r sits in lane
-// 32 (r / 16) + r % 16, so lanes 16..31 of each warp's quarter are unused.
-//
-// Every wait on an mbarrier is bounded; on timeout the CTA records
-// GDN_ETIMEOUT in the status word, stops issuing work, waits (bounded) for
-// its outstanding copies, frees its tensor memory and returns.
+// Tensor-memory layouts: an M=128 accumulator keeps row m in lane m; an M=64
+// accumulator keeps row r in lane 32 (r / 16) + r % 16.
+// Every mbarrier wait is bounded; on timeout the CTA records GDN_ETIMEOUT,
+// stops, drains its outstanding copies (bounded), frees TMEM and returns.
 #include <string.h>
 
 #include "gdn_common.cuh"
@@ -44,14 +48,19 @@ namespace {
 
 using namespace tc;
 
-constexpr int kTcThreads = 128;
-constexpr int kDvTile = 64;
-constexpr uint32_t kTile64 = 64 * 128;  // bytes of a [64][64] bf16 tile
-constexpr uint32_t kAPad = 68;          // f32 row pitch of the solve matrices
+constexpr uint32_t kTile = 64 * 128;  // bytes of a [64 rows][64 bf16] swizzled tile
+constexpr int kFPitch = 68;           // f32 row pitch of the solve matrices
+
+// per (chunk, v-head) outputs of the prepare kernel
+constexpr uint32_t kUnitAb = 0;               // A diag(beta)        [i][j]
+constexpr uint32_t kUnitW = kTile;            // -gamma_{c-1} W_c    [i][d], two d-halves
+constexpr uint32_t kUnitG = 3 * kTile;        // -G_{c-1}            [i][i']
+constexpr uint32_t kUnitP = 4 * kTile;        // P_c                 [r][i]
+constexpr uint32_t kUnitBytes = 5 * kTile;    // 40 KiB
 
 struct TcWs {
-    uint8_t *A;   // [max_chunks][hv][8 KiB]  A diag(beta), bf16, swizzled K-major
-    float *gb;    // [max_chunks][hv][128]    gc[0..63], beta[0..63]
+    uint8_t *unit;  // [max_chunks][hv][kUnitBytes]
+    float *gb;      // [max_chunks][hv][128]: gc[0..63], beta[0..63]
 };
 
 __host__ __device__ inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -60,8 +69,8 @@ TcWs tc_carve(void *base, int max_chunks, int hv) {
     char *p = static_cast<char *>(base);
     const size_t units = size_t(max_chunks) * hv;
     TcWs w;
-    w.A = reinterpret_cast<uint8_t *>(p);
-    p += al256(units * kTile64);
+    w.unit = reinterpret_cast<uint8_t *>(p);
+    p += al256(units * kUnitBytes);
     w.gb = reinterpret_cast<float *>(p);
     return w;
 }
@@ -71,71 +80,104 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-// writes 8 floats as one 16-byte chunk of bf16
-__device__ __forceinline__ void st_chunk_bf16(uint8_t *dst, const float *x) {
-    uint4 u;
-    u.x = pack_bf16x2(x[0], x[1]);
-    u.y = pack_bf16x2(x[2], x[3]);
-    u.z = pack_bf16x2(x[4], x[5]);
-    u.w = pack_bf16x2(x[6], x[7]);
-    *reinterpret_cast<uint4 *>(dst) = u;
+__device__ __forceinline__ uint4 pack8(const float *x) {
+    return make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                      pack_bf16x2(x[6], x[7]));
 }
 
-// row of an M=64 accumulator held by (warp, lane), or -1 for the unused lanes
-__device__ __forceinline__ int m64_row(int warp, int lane) { return lane < 16 ? warp * 16 + lane : -1; }
+__device__ __forceinline__ void unpack8(const uint4 u, float *x) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(h[q]);
+        x[2 * q] = f.x;
+        x[2 * q + 1] = f.y;
+    }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// inclusive prefix sum of 64 values held two per lane (lane l: 2l, 2l+1)
+__device__ __forceinline__ void warp_scan64(float &a0, float &a1, int lane) {
+    a1 += a0;
+    float s = a1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += t;
+    }
+    const float before = s - a1;
+    a0 += before;
+    a1 = s;
+}
 
 // ===========================================================================
 // k_chunk_prepare_tc
 // ===========================================================================
+constexpr int kPrepThreads = 256;
+
 struct PrepSmem {
-    alignas(1024) uint8_t K[2 * kTile64];  // K tile, two 64-column halves
-    float KK[64 * kAPad];                  // K K^T (f32)
-    float M[64 * kAPad];                   // masked, gated strict lower part
-    alignas(16) uint8_t At[kTile64];       // A diag(beta) bf16 swizzled (staging)
-    float gc[64], beta[64], graw[64];
+    alignas(1024) uint8_t KQ[4 * kTile];  // [K_c ; Q_c] K-major, M = 128: two d-halves of 16 KiB
+    alignas(1024) uint8_t Kp[2 * kTile];  // K_{c-1}, two d-halves
+    alignas(1024) uint8_t Ag[kTile];      // A diag(beta gamma) bf16 [i][j]
+    alignas(1024) uint8_t Wb[2 * kTile];  // W_c bf16 [i][d]
+    float M[64 * kFPitch];                // strict lower gated K K^T
+    float X[64 * kFPitch];                // (I + M)^-1
+    float T[3 * 256];                     // block products of the solve
+    float gc[64], beta[64], gcp[64], dprev[64];
     uint64_t bar_load, bar_mma;
     uint32_t tmem;
     int abort;
 };
 
-__global__ void __launch_bounds__(kTcThreads) k_chunk_prepare_tc(PrefillArgs a, TcWs w,
-                                                                  const __grid_constant__ CUtensorMap tm_k) {
+__global__ void __launch_bounds__(kPrepThreads, 2)
+k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm_q,
+                   const __grid_constant__ CUtensorMap tm_k) {
     extern __shared__ uint8_t smraw[];
     PrepSmem &s = *reinterpret_cast<PrepSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     const int c = blockIdx.x, hk = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (c >= *a.n_chunks) return;  // also covers a rejected chunk table (-1)
+    if (c >= *a.n_chunks) return;  // also a rejected chunk table (-1)
     const ChunkInfo ci = a.chunk_info[c];
     const int l = ci.len;
+    const bool has_prev = ci.idx > 0;
+    const int prev_start = ci.start - kChunk;
 
     if (tid == 0) {
         s.abort = 0;
         mbar_init(&s.bar_load, 1);
         mbar_init(&s.bar_mma, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(&s.bar_load, 2 * kTile64);
-        tma_load_3d(s.K, &tm_k, 0, hk, ci.start, &s.bar_load);
-        tma_load_3d(s.K + kTile64, &tm_k, 64, hk, ci.start, &s.bar_load);
+        mbar_arrive_expect_tx(&s.bar_load, (has_prev ? 6u : 4u) * kTile);
+        for (int hf = 0; hf < 2; ++hf) {
+            tma_load_3d(s.KQ + hf * 2 * kTile, &tm_k, 64 * hf, hk, ci.start, &s.bar_load);
+            tma_load_3d(s.KQ + hf * 2 * kTile + kTile, &tm_q, 64 * hf, hk, ci.start, &s.bar_load);
+            if (has_prev) tma_load_3d(s.Kp + hf * kTile, &tm_k, 64 * hf, hk, prev_start, &s.bar_load);
+        }
     }
     if (warp == 0) {
-        tmem_alloc(&s.tmem, 64);
+        tmem_alloc(&s.tmem, 256);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s.tmem;
+    const uint32_t kTmKK = 0, kTmW = 64, kTmG = 192;
+    uint32_t mma_phase = 0;
 
-    // K K^T (M=64, N=64, K=128): both operands K-major from the K tile
+    // [K;Q] K^T : M=128 (rows 0-63 K K^T, rows 64-127 Q K^T), N=64, K=128
     if (tid == 0) {
         if (mbar_wait(&s.bar_load, 0)) {
             tc_fence_after();
-            const uint32_t id = idesc_bf16_f32(64, 64, false, false);
-            const uint32_t kb = smem_u32(s.K);
+            const uint32_t kq = smem_u32(s.KQ);
+            const uint32_t id = idesc_bf16_f32(128, 64, false, false);
 #pragma unroll
-            for (int st = 0; st < 8; ++st) {
-                const uint32_t off = (st >> 2) * kTile64 + (st & 3) * 32;
-                mma_bf16(tmem, sdesc_sw128(kb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), id, st > 0);
+            for (int t = 0; t < 8; ++t) {
+                const uint32_t off = (t >> 2) * 2 * kTile + (t & 3) * 32;
+                mma_bf16(tmem + kTmKK, sdesc_sw128(kq + off, 16, 1024), sdesc_sw128(kq + off, 16, 1024), id, t > 0);
             }
             mma_commit(&s.bar_mma);
         } else {
@@ -143,150 +185,257 @@ __global__ void __launch_bounds__(kTcThreads) k_chunk_prepare_tc(PrefillArgs a, 
         }
     }
     __syncthreads();
-    bool ok = !s.abort;
-    if (ok && !mbar_wait(&s.bar_mma, 0)) s.abort = 1;
+    if (!s.abort && !mbar_wait(&s.bar_mma, mma_phase)) s.abort = 1;
+    mma_phase ^= 1;
     __syncthreads();
-    ok = !s.abort;
-    if (ok) {
-        tc_fence_after();
-        const int r = m64_row(warp, lane);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            float v[16];
-            tmem_ld16(tmem_addr(tmem, 32 * warp, 16 * j), v);
-            tmem_ld_wait();
-            if (r >= 0)
-#pragma unroll
-                for (int e = 0; e < 16; ++e) s.KK[r * kAPad + 16 * j + e] = v[e];
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
+    tc_fence_after();
 
-    for (int hh = 0; ok && hh < a.group; ++hh) {
+    const int q4 = warp & 3, colhalf = warp >> 2;
+    for (int hh = 0; !s.abort && hh < a.group; ++hh) {
         const int h = hk * a.group + hh;
         const size_t unit = size_t(c) * a.hv + h;
-        // chunk_gate_cumsum (left-to-right f32 sum, restarted at the chunk)
-        if (tid < 64) {
-            const bool in = tid < l;
-            s.graw[tid] = in ? a.g[size_t(ci.start + tid) * a.hv + h] : 0.f;
-            s.beta[tid] = in ? a.beta[size_t(ci.start + tid) * a.hv + h] : 0.f;
+        uint8_t *uo = w.unit + unit * kUnitBytes;
+        // ---- gate prefix sums (this chunk; previous chunk of the sequence) ----
+        if (warp < 2) {
+            const int base = warp == 0 ? ci.start : prev_start;
+            const int len = warp == 0 ? l : (has_prev ? kChunk : 0);
+            float a0 = 2 * lane < len ? a.g[size_t(base + 2 * lane) * a.hv + h] : 0.f;
+            float a1 = 2 * lane + 1 < len ? a.g[size_t(base + 2 * lane + 1) * a.hv + h] : 0.f;
+            warp_scan64(a0, a1, lane);
+            float *dst = warp == 0 ? s.gc : s.gcp;
+            dst[2 * lane] = a0;
+            dst[2 * lane + 1] = a1;
+        } else if (warp < 4) {
+            const int i = tid - 64;
+            s.beta[i] = i < l ? a.beta[size_t(ci.start + i) * a.hv + h] : 0.f;
         }
         __syncthreads();
         if (tid < 64) {
-            float run = 0.f;
-            for (int j = 0; j <= tid; ++j) run += s.graw[j];
-            s.gc[tid] = run;
-            w.gb[unit * 128 + tid] = run;
+            w.gb[unit * 128 + tid] = s.gc[tid];
             w.gb[unit * 128 + 64 + tid] = s.beta[tid];
+            s.dprev[tid] = has_prev ? __expf(s.gcp[63] - s.gcp[tid]) : 0.f;
         }
-        __syncthreads();
-        // M = StrictLower(B Gamma K K^T Gamma^-1) on the valid block
-        for (int e = tid; e < 64 * 64; e += kTcThreads) {
-            const int i = e >> 6, j = e & 63;
-            float m = 0.f;
-            if (j < i && i < l) m = s.beta[i] * __expf(s.gc[i] - s.gc[j]) * s.KK[i * kAPad + j];
-            s.M[i * kAPad + j] = m;
-        }
-        __syncthreads();
-        // A = (I + M)^-1: thread j solves column j, keeping it in registers;
-        // rows i < j of column j are zero (A is unit lower triangular)
-        if (tid < 64) {
-            const int j = tid;
-            float col[64];
+        // ---- M (from K K^T) and P (from Q K^T), straight out of TMEM ----
+        {
+            float v[32];
+            tmem_ld16(tmem_addr(tmem, 32 * q4, kTmKK + 32 * colhalf), v);
+            tmem_ld16(tmem_addr(tmem, 32 * q4, kTmKK + 32 * colhalf + 16), v + 16);
+            tmem_ld_wait();
+            if (q4 < 2) {
+                const int i = 32 * q4 + lane;
+                const float bi = s.beta[i], gi = s.gc[i];
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                float x0 = (i == j) ? 1.f : 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
-                const float *Mi = s.M + i * kAPad;
+                for (int e = 0; e < 32; ++e) {
+                    const int j = 32 * colhalf + e;
+                    s.M[i * kFPitch + j] = (j < i && i < l) ? bi * __expf(gi - s.gc[j]) * v[e] : 0.f;
+                }
+            } else {
+                const int r = 32 * (q4 - 2) + lane;
+                const float gr = s.gc[r];
 #pragma unroll
-                for (int m = 0; m + 3 < i; m += 4) {
-                    const float4 mm = *reinterpret_cast<const float4 *>(Mi + m);
-                    x0 = fmaf(-mm.x, col[m], x0);
-                    x1 = fmaf(-mm.y, col[m + 1], x1);
-                    x2 = fmaf(-mm.z, col[m + 2], x2);
-                    x3 = fmaf(-mm.w, col[m + 3], x3);
+                for (int e = 0; e < 32; ++e) {
+                    const int i = 32 * colhalf + e;
+                    v[e] = (i <= r && r < l) ? __expf(gr - s.gc[i]) * v[e] : 0.f;
                 }
 #pragma unroll
-                for (int m = i & ~3; m < i; ++m) x0 = fmaf(-Mi[m], col[m], x0);
-                col[i] = (j < l && i < l) ? (x0 + x1) + (x2 + x3) : 0.f;
-            }
-            // A diag(beta): column j scaled by beta_j, into the swizzled tile
-            const float bj = s.beta[j];
-            const int chunk = j >> 3, sub = j & 7;
-#pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                const __nv_bfloat16 v = __float2bfloat16_rn(col[i] * bj);
-                *reinterpret_cast<__nv_bfloat16 *>(s.At + sw128_offset(i, chunk) + 2 * sub) = v;
+                for (int q = 0; q < 4; ++q)
+                    *reinterpret_cast<uint4 *>(uo + kUnitP + sw128_offset(r, 4 * colhalf + q)) = pack8(v + 8 * q);
             }
         }
         __syncthreads();
-        uint4 *dst = reinterpret_cast<uint4 *>(w.A + unit * kTile64);
-        const uint4 *src = reinterpret_cast<const uint4 *>(s.At);
-        for (int e = tid; e < int(kTile64 / 16); e += kTcThreads) dst[e] = src[e];
+        // ---- A = (I + M)^-1, blocked 16x16 forward substitution ----
+        if (tid < 64) {  // diagonal blocks: thread = (block, column)
+            const int b = tid >> 4, jj = tid & 15;
+            float x[16];
+#pragma unroll
+            for (int ii = 0; ii < 16; ++ii) {
+                float acc = (ii == jj) ? 1.f : 0.f;
+                const float *Mr = s.M + (16 * b + ii) * kFPitch + 16 * b;
+#pragma unroll
+                for (int m = 0; m < ii; ++m) acc = fmaf(-Mr[m], x[m], acc);
+                x[ii] = acc;
+            }
+#pragma unroll
+            for (int ii = 0; ii < 16; ++ii) s.X[(16 * b + ii) * kFPitch + 16 * b + jj] = x[ii];
+        } else {  // zero the strictly-upper blocks
+            for (int e = tid - 64; e < 6 * 256; e += kPrepThreads - 64) {
+                const int blk = e >> 8, ii = (e >> 4) & 15, jj = e & 15;
+                const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+                const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+                s.X[(16 * bi + ii) * kFPitch + 16 * bj + jj] = 0.f;
+            }
+        }
+        __syncthreads();
+        {
+            const int ii = tid >> 4, jj = tid & 15;
+#pragma unroll
+            for (int L = 1; L < 4; ++L) {
+                for (int j = 0; j + L < 4; ++j) {  // T = sum_{k=j}^{i-1} M_ik X_kj
+                    const int i = j + L;
+                    float acc = 0.f;
+                    for (int k = j; k < i; ++k) {
+                        const float *Mr = s.M + (16 * i + ii) * kFPitch + 16 * k;
+                        const float *Xc = s.X + (16 * k) * kFPitch + 16 * j + jj;
+#pragma unroll
+                        for (int m = 0; m < 16; ++m) acc = fmaf(Mr[m], Xc[m * kFPitch], acc);
+                    }
+                    s.T[j * 256 + tid] = acc;
+                }
+                __syncthreads();
+                for (int j = 0; j + L < 4; ++j) {  // X_ij = -X_ii T
+                    const int i = j + L;
+                    const float *Xr = s.X + (16 * i + ii) * kFPitch + 16 * i;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int m = 0; m < 16; ++m)
+                        if (m <= ii) acc = fmaf(Xr[m], s.T[j * 256 + m * 16 + jj], acc);
+                    s.X[(16 * i + ii) * kFPitch + 16 * j + jj] = -acc;
+                }
+                __syncthreads();
+            }
+        }
+        // ---- A diag(beta) -> global; A diag(beta gamma) -> smem operand ----
+        for (int p = tid; p < 512; p += kPrepThreads) {
+            const int i = p >> 3, ch = p & 7;
+            float x[8], y[8];
+            const float4 *xr = reinterpret_cast<const float4 *>(s.X + i * kFPitch + 8 * ch);
+            const float4 x0 = xr[0], x1 = xr[1];
+            x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
+            x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int j = 8 * ch + e;
+                x[e] *= s.beta[j];
+                y[e] = x[e] * __expf(s.gc[j]);
+            }
+            *reinterpret_cast<uint4 *>(uo + kUnitAb + sw128_offset(i, ch)) = pack8(x);
+            *reinterpret_cast<uint4 *>(s.Ag + sw128_offset(i, ch)) = pack8(y);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // ---- W_c = Ag K_c : M=64, N=128 (d), K=64 (j); K tile read MN-major ----
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t ag = smem_u32(s.Ag), kq = smem_u32(s.KQ);
+            const uint32_t id = idesc_bf16_f32(64, 128, false, true);
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                mma_bf16(tmem + kTmW, sdesc_sw128(ag + 32 * t, 16, 1024), sdesc_sw128(kq + 2048 * t, 2 * kTile, 1024),
+                         id, t > 0);
+            mma_commit(&s.bar_mma);
+        }
+        if (!mbar_wait(&s.bar_mma, mma_phase)) s.abort = 1;
+        mma_phase ^= 1;
+        tc_fence_after();
+        {
+            const float gprev = has_prev ? -__expf(s.gcp[63]) : -1.f;
+            const int i = 16 * q4 + lane;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float v[16];
+                tmem_ld16(tmem_addr(tmem, 32 * q4, kTmW + 64 * colhalf + 16 * j), v);
+                tmem_ld_wait();
+                if (lane < 16) {
+                    uint8_t *wbh = s.Wb + colhalf * kTile;
+                    uint8_t *woh = uo + kUnitW + colhalf * kTile;
+                    float sv[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) sv[e] = gprev * v[e];
+                    *reinterpret_cast<uint4 *>(wbh + sw128_offset(i, 2 * j)) = pack8(v);
+                    *reinterpret_cast<uint4 *>(wbh + sw128_offset(i, 2 * j + 1)) = pack8(v + 8);
+                    *reinterpret_cast<uint4 *>(woh + sw128_offset(i, 2 * j)) = pack8(sv);
+                    *reinterpret_cast<uint4 *>(woh + sw128_offset(i, 2 * j + 1)) = pack8(sv + 8);
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // ---- G_{c-1} = W_c K_{c-1}^T diag(d_{c-1}) : M=64, N=64, K=128 ----
+        if (has_prev) {
+            if (tid == 0) {
+                tc_fence_after();
+                const uint32_t wb = smem_u32(s.Wb), kp = smem_u32(s.Kp);
+                const uint32_t id = idesc_bf16_f32(64, 64, false, false);
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    const uint32_t off = (t >> 2) * kTile + (t & 3) * 32;
+                    mma_bf16(tmem + kTmG, sdesc_sw128(wb + off, 16, 1024), sdesc_sw128(kp + off, 16, 1024), id, t > 0);
+                }
+                mma_commit(&s.bar_mma);
+            }
+            if (!mbar_wait(&s.bar_mma, mma_phase)) s.abort = 1;
+            mma_phase ^= 1;
+            tc_fence_after();
+            const int i = 16 * q4 + lane;
+            float v[32];
+            tmem_ld16(tmem_addr(tmem, 32 * q4, kTmG + 32 * colhalf), v);
+            tmem_ld16(tmem_addr(tmem, 32 * q4, kTmG + 32 * colhalf + 16), v + 16);
+            tmem_ld_wait();
+            if (lane < 16) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[e] = -v[e] * s.dprev[32 * colhalf + e];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    *reinterpret_cast<uint4 *>(uo + kUnitG + sw128_offset(i, 4 * colhalf + q)) = pack8(v + 8 * q);
+            }
+        } else {
+            for (int p = tid; p < int(kTile / 16); p += kPrepThreads)
+                reinterpret_cast<uint4 *>(uo + kUnitG)[p] = make_uint4(0, 0, 0, 0);
+        }
+        tc_fence_before();
         __syncthreads();
     }
     if (s.abort && tid == 0) {
         record_status(a.status, GDN_ETIMEOUT);
-        mbar_wait(&s.bar_load, 0, 100000000ull);  // bounded drain of the K-tile copy
+        mbar_wait(&s.bar_load, 0, 100000000ull);  // bounded drain of the tile copies
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 64);
+    if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
 // ===========================================================================
 // k_chunk_state_output_tc
 // ===========================================================================
-struct Stage {
-    alignas(1024) uint8_t Q[2 * kTile64];
-    uint8_t K[2 * kTile64];
-    uint8_t V[kTile64];
-    uint8_t A[kTile64];
-    float gb[128];
+constexpr int kMathThreads = 128;
+constexpr int kStateThreads = 192;  // 4 math warps + producer warp + MMA warp
+constexpr int kDvTile = 64;
+
+struct StepBuf {
+    alignas(1024) uint8_t A0[2 * kTile];  // [A_{c+1} B ; 0]          K-major, M=128, K=64
+    alignas(1024) uint8_t A1[4 * kTile];  // [-W'_{c+1} ; Gamma_c Q_c] K-major, M=128, K=128 (two d-halves)
+    alignas(1024) uint8_t A2[2 * kTile];  // [-G_c ; P_c]             K-major, M=128, K=64
+    alignas(1024) uint8_t Bv[kTile];      // V_{c+1}[:, tile]         MN-major B, [j][e]
+    alignas(1024) uint8_t Kt[2 * kTile];  // K_c                      MN-major A (K^T), [i][d]
+    float gbc[128];                       // gc, beta of chunk c
+    float gbn[128];                       // gc, beta of chunk c+1
 };
 
 struct StateSmem {
-    Stage st[2];
-    alignas(1024) uint8_t Ag[kTile64];    // A diag(beta gamma), K-major [i][j]
-    uint8_t W[2 * kTile64];               // W bf16, K-major [i][d]
-    uint8_t P[kTile64];                   // masked decayed Q K^T, K-major [r][i]
-    uint8_t S[2 * kTile64];               // state bf16 [d][e] (128 rows), MN-major B
-    uint8_t Vp[kTile64];                  // V' bf16 [i][e], MN-major B
-    uint8_t Vd[kTile64];                  // diag(gamma_l/gamma_i) V' bf16 [i][e]
-    uint64_t bar_load[2], bar_mma;
+    StepBuf buf[2];
+    alignas(1024) uint8_t Sb[2 * kTile];  // S_c bf16 [d][e] (128 rows), MN-major B
+    alignas(1024) uint8_t Vp[kTile];      // V'_c bf16 [i][e], MN-major B
+    alignas(1024) uint8_t Vd[kTile];      // diag(d_c) V'_c bf16 [i][e], MN-major B
+    uint64_t full[2], empty[2], ready, mma;
     uint32_t tmem;
     int abort;
 };
-
-// tensor-memory columns of the accumulators (512 allocated)
-constexpr uint32_t kColW = 0, kColU = 128, kColP = 192, kColWS = 256, kColQS = 320, kColPV = 384, kColKV = 448;
-constexpr uint32_t kStageBytes = 2 * kTile64 + 2 * kTile64 + kTile64 + kTile64 + 512;
 
 struct StateArgs {
     PrefillArgs a;
     TcWs w;
 };
 
-__device__ __forceinline__ void issue_stage_loads(StateSmem &s, int stage, const PrefillArgs &a, const TcWs &w,
-                                                  const CUtensorMap *tq, const CUtensorMap *tk,
-                                                  const CUtensorMap *tv, int c, int h, int hk, int e0) {
-    const ChunkInfo ci = a.chunk_info[c];
-    Stage &st = s.st[stage];
-    uint64_t *bar = &s.bar_load[stage];
-    const size_t unit = size_t(c) * a.hv + h;
-    mbar_arrive_expect_tx(bar, kStageBytes);
-    tma_load_3d(st.Q, tq, 0, hk, ci.start, bar);
-    tma_load_3d(st.Q + kTile64, tq, 64, hk, ci.start, bar);
-    tma_load_3d(st.K, tk, 0, hk, ci.start, bar);
-    tma_load_3d(st.K + kTile64, tk, 64, hk, ci.start, bar);
-    tma_load_3d(st.V, tv, e0, h, ci.start, bar);
-    bulk_load(st.A, w.A + unit * kTile64, kTile64, bar);
-    bulk_load(st.gb, w.gb + unit * 128, 512, bar);
-}
+// dynamic shared memory per block is capped at 227 KiB; one more KiB is
+// requested to align the base to 1024 bytes
+static_assert(sizeof(StateSmem) + 1024 <= 227 * 1024, "state kernel shared memory");
+static_assert(2 * (sizeof(PrepSmem) + 1024) <= 228 * 1024, "two prepare CTAs per SM");
 
-__global__ void __launch_bounds__(kTcThreads, 1)
-k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v) {
+__global__ void __launch_bounds__(kStateThreads, 1)
+k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
     extern __shared__ uint8_t smraw[];
     StateSmem &s = *reinterpret_cast<StateSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     const PrefillArgs &a = sa.a;
@@ -296,269 +445,240 @@ k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q, 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (*a.n_chunks < 0) return;  // the chunk table rejected cu_seqlens
     const SeqInfo si = a.seq_info[n];
+    const int nc = si.num_chunks;
     const size_t sbase = (size_t(n) * a.hv + h) * kHeadDim * kHeadDim;
 
+    // zero every operand buffer once: regions a step does not load must hold
+    // finite values (their products land in rows that are discarded)
+    for (uint32_t o = tid * 16; o < sizeof(StateSmem) - 64; o += kStateThreads * 16)
+        *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(&s) + o) = make_uint4(0, 0, 0, 0);
+    __syncthreads();
     if (tid == 0) {
         s.abort = 0;
-        mbar_init(&s.bar_load[0], 1);
-        mbar_init(&s.bar_load[1], 1);
-        mbar_init(&s.bar_mma, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&s.full[b], 1);
+            mbar_init(&s.empty[b], 1);
+        }
+        mbar_init(&s.ready, kMathThreads);
+        mbar_init(&s.mma, 1);
         fence_mbar_init();
-        prefetch_tensormap(&tm_q);
-        prefetch_tensormap(&tm_k);
-        prefetch_tensormap(&tm_v);
-        if (si.num_chunks > 0) issue_stage_loads(s, 0, a, w, &tm_q, &tm_k, &tm_v, si.first_chunk, h, hk, e0);
     }
     if (warp == 0) {
-        tmem_alloc(&s.tmem, 512);
+        tmem_alloc(&s.tmem, 128);
         tmem_relinquish();
     }
-    // initial state row d = tid (64 columns of this tile) in registers
+    // initial state rows (thread t = row d = t) and its bf16 operand copy
     float Sr[64];
+    if (tid < kMathThreads) {
 #pragma unroll
-    for (int q = 0; q < 64; ++q) Sr[q] = 0.f;
-    if (a.s0) {
-        const float4 *src = reinterpret_cast<const float4 *>(a.s0 + sbase + size_t(tid) * kHeadDim + e0);
+        for (int q = 0; q < 64; ++q) Sr[q] = 0.f;
+        if (a.s0) {
+            const float4 *src = reinterpret_cast<const float4 *>(a.s0 + sbase + size_t(tid) * kHeadDim + e0);
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-            const float4 v = src[q];
-            Sr[4 * q] = v.x; Sr[4 * q + 1] = v.y; Sr[4 * q + 2] = v.z; Sr[4 * q + 3] = v.w;
+            for (int q = 0; q < 16; ++q) {
+                const float4 v = src[q];
+                Sr[4 * q] = v.x; Sr[4 * q + 1] = v.y; Sr[4 * q + 2] = v.z; Sr[4 * q + 3] = v.w;
+            }
         }
-    }
-    // bf16 copy of the state as the MN-major B operand: row d = tid of a
-    // [128][64] tile of 128-byte rows
-    auto write_state = [&]() {
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) st_chunk_bf16(s.S + sw128_offset(tid, ch), Sr + 8 * ch);
-    };
-    write_state();
+        for (int ch = 0; ch < 8; ++ch)
+            *reinterpret_cast<uint4 *>(s.Sb + sw128_offset(tid, ch)) = pack8(Sr + 8 * ch);
+    }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s.tmem;
-    uint32_t mma_phase = 0;
-    const int r64 = m64_row(warp, lane);
+    const uint32_t kTmD1 = 0, kTmD2 = 64;
 
-    const uint32_t id_w = idesc_bf16_f32(64, 128, false, true);   // A K-major, B MN-major
-    const uint32_t id_u = idesc_bf16_f32(64, 64, false, true);
-    const uint32_t id_qk = idesc_bf16_f32(64, 64, false, false);  // both K-major
-    const uint32_t id_kv = idesc_bf16_f32(128, 64, true, true);   // both MN-major
-
-    for (int cc = 0; cc < si.num_chunks && !s.abort; ++cc) {
-        const int c = si.first_chunk + cc;
-        const int stg = cc & 1;
-        Stage &st = s.st[stg];
-        const ChunkInfo ci = a.chunk_info[c];
-        const int l = ci.len;
-        // prefetch the next chunk into the other stage (its previous user,
-        // chunk cc-1, has finished every MMA that read it)
-        if (tid == 0 && cc + 1 < si.num_chunks)
-            issue_stage_loads(s, stg ^ 1, a, w, &tm_q, &tm_k, &tm_v, c + 1, h, hk, e0);
-        if (!mbar_wait(&s.bar_load[stg], (cc >> 1) & 1)) s.abort = 1;
-        __syncthreads();
-        if (s.abort) break;
-
-        // A diag(beta gamma) = A diag(beta) scaled by gamma_j per column
-        for (int e = tid; e < 64 * 8; e += kTcThreads) {
-            const int i = e >> 3, ch = e & 7;
-            const uint32_t off = sw128_offset(i, ch);
-            const uint4 u = *reinterpret_cast<const uint4 *>(st.A + off);
-            const __nv_bfloat16 *b = reinterpret_cast<const __nv_bfloat16 *>(&u);
-            float x[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) x[q] = __bfloat162float(b[q]) * __expf(st.gb[8 * ch + q]);
-            st_chunk_bf16(s.Ag + off, x);
-        }
-        fence_proxy_async_smem();
-        __syncthreads();
-
-        // MMA group 1: W, U, Q K^T, Q S
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t q = smem_u32(st.Q), k = smem_u32(st.K), v = smem_u32(st.V), A = smem_u32(st.A);
-            const uint32_t ag = smem_u32(s.Ag), S = smem_u32(s.S);
-#pragma unroll
-            for (int t = 0; t < 4; ++t)  // W = Ag K : K over chunk positions
-                mma_bf16(tmem + kColW, sdesc_sw128(ag + 32 * t, 16, 1024), sdesc_sw128(k + 2048 * t, kTile64, 1024),
-                         id_w, t > 0);
-#pragma unroll
-            for (int t = 0; t < 4; ++t)  // U = A V
-                mma_bf16(tmem + kColU, sdesc_sw128(A + 32 * t, 16, 1024), sdesc_sw128(v + 2048 * t, kTile64, 1024),
-                         id_u, t > 0);
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {  // Q K^T and Q S : K over d
-                const uint32_t off = (t >> 2) * kTile64 + (t & 3) * 32;
-                mma_bf16(tmem + kColP, sdesc_sw128(q + off, 16, 1024), sdesc_sw128(k + off, 16, 1024), id_qk, t > 0);
-                mma_bf16(tmem + kColQS, sdesc_sw128(q + off, 16, 1024), sdesc_sw128(S + 2048 * t, kTile64, 1024),
-                         id_u, t > 0);
-            }
-            mma_commit(&s.bar_mma);
-        }
-        if (!mbar_wait(&s.bar_mma, mma_phase)) s.abort = 1;
-        mma_phase ^= 1;
-        tc_fence_after();
-
-        // epilogue 1: W -> bf16 operand; P = masked, decayed Q K^T -> bf16
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float v[16];
-            tmem_ld16(tmem_addr(tmem, 32 * warp, kColW + 16 * j), v);
-            tmem_ld_wait();
-            if (r64 >= 0) {
-                uint8_t *half = s.W + (j >> 2) * kTile64;
-                st_chunk_bf16(half + sw128_offset(r64, (2 * j) & 7), v);
-                st_chunk_bf16(half + sw128_offset(r64, (2 * j + 1) & 7), v + 8);
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            float v[16];
-            tmem_ld16(tmem_addr(tmem, 32 * warp, kColP + 16 * j), v);
-            tmem_ld_wait();
-            if (r64 >= 0) {
-                const float gr = st.gb[r64];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int i = 16 * j + e;
-                    v[e] = (i <= r64 && r64 < l) ? __expf(gr - st.gb[i]) * v[e] : 0.f;
+    if (warp == 4) {
+        // ----------------------------- producer -----------------------------
+        if (lane == 0 && nc > 0) {
+            prefetch_tensormap(&tm_q);
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+            for (int c = -1; c < nc && !s.abort; ++c) {
+                const int b = (c + 1) & 1, use = (c + 1) >> 1;
+                if (use > 0 && !mbar_wait(&s.empty[b], (use - 1) & 1)) {
+                    s.abort = 1;
+                    break;
                 }
-                st_chunk_bf16(s.P + sw128_offset(r64, 2 * j), v);
-                st_chunk_bf16(s.P + sw128_offset(r64, 2 * j + 1), v + 8);
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (s.abort) break;
-
-        // MMA group 2: W S
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t Wb = smem_u32(s.W), S = smem_u32(s.S);
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const uint32_t off = (t >> 2) * kTile64 + (t & 3) * 32;
-                mma_bf16(tmem + kColWS, sdesc_sw128(Wb + off, 16, 1024), sdesc_sw128(S + 2048 * t, kTile64, 1024),
-                         id_u, t > 0);
-            }
-            mma_commit(&s.bar_mma);
-        }
-        if (!mbar_wait(&s.bar_mma, mma_phase)) s.abort = 1;
-        mma_phase ^= 1;
-        tc_fence_after();
-
-        // epilogue 2: V' = U - W S ; Vd = diag(gamma_l / gamma_i) V'
-        {
-            const float gl = st.gb[l - 1];
-            const float di = (r64 >= 0 && r64 < l) ? __expf(gl - st.gb[r64]) : 0.f;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float u[16], ws[16];
-                tmem_ld16(tmem_addr(tmem, 32 * warp, kColU + 16 * j), u);
-                tmem_ld16(tmem_addr(tmem, 32 * warp, kColWS + 16 * j), ws);
-                tmem_ld_wait();
-                if (r64 >= 0) {
-                    float vp[16], vd[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        vp[e] = u[e] - ws[e];
-                        vd[e] = di * vp[e];
+                StepBuf &B = s.buf[b];
+                uint32_t bytes = 0;
+                const bool cur = c >= 0, nxt = c + 1 < nc;
+                if (cur) bytes += 2 * kTile /*Q*/ + kTile /*P*/ + 2 * kTile /*K*/ + 512;
+                if (nxt) bytes += kTile /*Ab*/ + 2 * kTile /*W*/ + kTile /*G*/ + kTile /*V*/ + 512;
+                mbar_arrive_expect_tx(&s.full[b], bytes);
+                if (cur) {
+                    const int cg = si.first_chunk + c;
+                    const ChunkInfo ci = a.chunk_info[cg];
+                    const uint8_t *uo = w.unit + (size_t(cg) * a.hv + h) * kUnitBytes;
+                    for (int hf = 0; hf < 2; ++hf) {
+                        tma_load_3d(B.A1 + hf * 2 * kTile + kTile, &tm_q, 64 * hf, hk, ci.start, &s.full[b]);
+                        tma_load_3d(B.Kt + hf * kTile, &tm_k, 64 * hf, hk, ci.start, &s.full[b]);
                     }
-                    st_chunk_bf16(s.Vp + sw128_offset(r64, 2 * j), vp);
-                    st_chunk_bf16(s.Vp + sw128_offset(r64, 2 * j + 1), vp + 8);
-                    st_chunk_bf16(s.Vd + sw128_offset(r64, 2 * j), vd);
-                    st_chunk_bf16(s.Vd + sw128_offset(r64, 2 * j + 1), vd + 8);
+                    bulk_load(B.A2 + kTile, uo + kUnitP, kTile, &s.full[b]);
+                    bulk_load(B.gbc, w.gb + (size_t(cg) * a.hv + h) * 128, 512, &s.full[b]);
+                }
+                if (nxt) {
+                    const int cg = si.first_chunk + c + 1;
+                    const ChunkInfo ci = a.chunk_info[cg];
+                    const uint8_t *uo = w.unit + (size_t(cg) * a.hv + h) * kUnitBytes;
+                    bulk_load(B.A0, uo + kUnitAb, kTile, &s.full[b]);
+                    bulk_load(B.A1, uo + kUnitW, kTile, &s.full[b]);
+                    bulk_load(B.A1 + 2 * kTile, uo + kUnitW + kTile, kTile, &s.full[b]);
+                    bulk_load(B.A2, uo + kUnitG, kTile, &s.full[b]);
+                    tma_load_3d(B.Bv, &tm_v, e0, h, ci.start, &s.full[b]);
+                    bulk_load(B.gbn, w.gb + (size_t(cg) * a.hv + h) * 128, 512, &s.full[b]);
                 }
             }
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        if (s.abort) break;
-
-        // MMA group 3: P V' and K^T Vd
-        if (tid == 0) {
+    } else if (warp == 5) {
+        // ---------------------------- MMA issuer ----------------------------
+        if (lane == 0 && nc > 0) {
+            const uint32_t id_kmn = idesc_bf16_f32(128, 64, false, true);
+            const uint32_t id_mnmn = idesc_bf16_f32(128, 64, true, true);
+            const uint32_t sb = smem_u32(s.Sb), vp = smem_u32(s.Vp), vd = smem_u32(s.Vd);
+            for (int c = -1; c < nc && !s.abort; ++c) {
+                const int b = (c + 1) & 1;
+                if (!mbar_wait(&s.ready, (c + 1) & 1)) {
+                    s.abort = 1;
+                    break;
+                }
+                tc_fence_after();
+                StepBuf &B = s.buf[b];
+                const uint32_t a0 = smem_u32(B.A0), a1 = smem_u32(B.A1), a2 = smem_u32(B.A2);
+                const uint32_t bv = smem_u32(B.Bv), kt = smem_u32(B.Kt);
+#pragma unroll
+                for (int t = 0; t < 4; ++t)  // [A B ; 0] V_{c+1}
+                    mma_bf16(tmem + kTmD1, sdesc_sw128(a0 + 32 * t, 16, 1024), sdesc_sw128(bv + 2048 * t, kTile, 1024),
+                             id_kmn, t > 0);
+#pragma unroll
+                for (int t = 0; t < 8; ++t)  // [-W' ; Gamma Q] S_c
+                    mma_bf16(tmem + kTmD1, sdesc_sw128(a1 + (t >> 2) * 2 * kTile + (t & 3) * 32, 16, 1024),
+                             sdesc_sw128(sb + 2048 * t, kTile, 1024), id_kmn, 1);
+#pragma unroll
+                for (int t = 0; t < 4; ++t)  // [-G ; P] V'_c
+                    mma_bf16(tmem + kTmD1, sdesc_sw128(a2 + 32 * t, 16, 1024), sdesc_sw128(vp + 2048 * t, kTile, 1024),
+                             id_kmn, 1);
+#pragma unroll
+                for (int t = 0; t < 4; ++t)  // K_c^T diag(d_c) V'_c
+                    mma_bf16(tmem + kTmD2, sdesc_sw128(kt + 2048 * t, kTile, 1024),
+                             sdesc_sw128(vd + 2048 * t, kTile, 1024), id_mnmn, t > 0);
+                mma_commit(&s.mma);
+                mma_commit(&s.empty[b]);
+            }
+        }
+    } else {
+        // --------------------------- math warps ----------------------------
+        const int t = tid;  // TMEM lane and state row
+        // an empty sequence has no steps at all (not even the virtual c = -1):
+        // its final state is its initial state
+        for (int c = -1; nc > 0 && c < nc && !s.abort; ++c) {
+            const int b = (c + 1) & 1, use = (c + 1) >> 1;
+            StepBuf &B = s.buf[b];
+            if (!mbar_wait(&s.full[b], use & 1)) {
+                s.abort = 1;
+                break;
+            }
+            // Gamma_c Q_c in place (rows 64..127 of A1), then hand over
+            if (c >= 0) {
+#pragma unroll
+                for (int k2 = 0; k2 < 8; ++k2) {
+                    const int p = t + kMathThreads * k2;  // 1024 chunks: 64 rows x 16
+                    const int r = p >> 4, hf = (p >> 3) & 1, ch = p & 7;
+                    uint8_t *ptr = B.A1 + hf * 2 * kTile + kTile + sw128_offset(r, ch);
+                    float x[8];
+                    unpack8(*reinterpret_cast<const uint4 *>(ptr), x);
+                    const float gr = __expf(B.gbc[r]);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] *= gr;
+                    *reinterpret_cast<uint4 *>(ptr) = pack8(x);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&s.ready);
+            if (!mbar_wait(&s.mma, (c + 1) & 1)) {
+                s.abort = 1;
+                break;
+            }
             tc_fence_after();
-            const uint32_t P = smem_u32(s.P), vp = smem_u32(s.Vp), vd = smem_u32(s.Vd), k = smem_u32(st.K);
+            // state update: S_{c+1}[t] = gamma_c S_c[t] + D2[t]
+            {
+                const int lc = c >= 0 ? a.chunk_info[si.first_chunk + c].len : 0;
+                const float gam = c >= 0 ? __expf(B.gbc[lc - 1]) : 1.f;
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                mma_bf16(tmem + kColPV, sdesc_sw128(P + 32 * t, 16, 1024), sdesc_sw128(vp + 2048 * t, kTile64, 1024),
-                         id_u, t > 0);
-                mma_bf16(tmem + kColKV, sdesc_sw128(k + 2048 * t, kTile64, 1024),
-                         sdesc_sw128(vd + 2048 * t, kTile64, 1024), id_kv, t > 0);
+                for (int j = 0; j < 4; ++j) {
+                    float v[16];
+                    tmem_ld16(tmem_addr(tmem, 32 * warp, kTmD2 + 16 * j), v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) Sr[16 * j + e] = fmaf(gam, Sr[16 * j + e], v[e]);
+                }
             }
-            mma_commit(&s.bar_mma);
-        }
-        if (!mbar_wait(&s.bar_mma, mma_phase)) s.abort = 1;
-        mma_phase ^= 1;
-        tc_fence_after();
-
-        // epilogue 3: state update (row d = tid), output rows r < l
-        {
-            const float gl = __expf(st.gb[l - 1]);
+            // D1 rows: V'_{c+1} (t < 64) or O_c (t >= 64)
+            float d1[64];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float kv[16];
-                tmem_ld16(tmem_addr(tmem, 32 * warp, kColKV + 16 * j), kv);
-                tmem_ld_wait();
+            for (int j = 0; j < 4; ++j) tmem_ld16(tmem_addr(tmem, 32 * warp, kTmD1 + 16 * j), d1 + 16 * j);
+            tmem_ld_wait();
+            tc_fence_before();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) Sr[16 * j + e] = fmaf(gl, Sr[16 * j + e], kv[e]);
-            }
-            const float gr = r64 >= 0 ? __expf(st.gb[r64]) : 0.f;
-            __nv_bfloat16 *orow =
-                r64 >= 0 ? static_cast<__nv_bfloat16 *>(a.out) + (size_t(ci.start + r64) * a.hv + h) * kHeadDim + e0
-                         : nullptr;
+            for (int ch = 0; ch < 8; ++ch)
+                *reinterpret_cast<uint4 *>(s.Sb + sw128_offset(t, ch)) = pack8(Sr + 8 * ch);
+            if (t < 64) {
+                if (c + 1 < nc) {
+                    const int ln = a.chunk_info[si.first_chunk + c + 1].len;
+                    const float dn = t < ln ? __expf(B.gbn[ln - 1] - B.gbn[t]) : 0.f;
+                    float vd[8];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float qs[16], pv[16];
-                tmem_ld16(tmem_addr(tmem, 32 * warp, kColQS + 16 * j), qs);
-                tmem_ld16(tmem_addr(tmem, 32 * warp, kColPV + 16 * j), pv);
-                tmem_ld_wait();
-                if (r64 >= 0 && r64 < l) {
-                    float o[16];
+                    for (int ch = 0; ch < 8; ++ch) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) o[e] = a.scale * fmaf(gr, qs[e], pv[e]);
-                    uint4 u0, u1;
-                    u0.x = pack_bf16x2(o[0], o[1]);   u0.y = pack_bf16x2(o[2], o[3]);
-                    u0.z = pack_bf16x2(o[4], o[5]);   u0.w = pack_bf16x2(o[6], o[7]);
-                    u1.x = pack_bf16x2(o[8], o[9]);   u1.y = pack_bf16x2(o[10], o[11]);
-                    u1.z = pack_bf16x2(o[12], o[13]); u1.w = pack_bf16x2(o[14], o[15]);
-                    reinterpret_cast<uint4 *>(orow + 16 * j)[0] = u0;
-                    reinterpret_cast<uint4 *>(orow + 16 * j)[1] = u1;
+                        for (int e = 0; e < 8; ++e) vd[e] = dn * d1[8 * ch + e];
+                        *reinterpret_cast<uint4 *>(s.Vp + sw128_offset(t, ch)) = pack8(d1 + 8 * ch);
+                        *reinterpret_cast<uint4 *>(s.Vd + sw128_offset(t, ch)) = pack8(vd);
+                    }
+                }
+            } else if (c >= 0) {
+                const int r = t - 64;
+                const ChunkInfo ci = a.chunk_info[si.first_chunk + c];
+                if (r < ci.len) {
+                    __nv_bfloat16 *orow =
+                        static_cast<__nv_bfloat16 *>(a.out) + (size_t(ci.start + r) * a.hv + h) * kHeadDim + e0;
+                    float o[8];
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) o[e] = a.scale * d1[8 * ch + e];
+                        reinterpret_cast<uint4 *>(orow)[ch] = pack8(o);
+                    }
                 }
             }
         }
-        tc_fence_before();
-        __syncthreads();  // every thread is done reading S (bf16) and TMEM
-        write_state();
-        fence_proxy_async_smem();
-        __syncthreads();
-    }
-
-    if (s.abort) {
-        if (tid == 0) {
-            record_status(a.status, GDN_ETIMEOUT);
-            // drain loads that may still be in flight into either stage
-            mbar_wait(&s.bar_load[0], 0, 100000000ull);
-            mbar_wait(&s.bar_load[1], 0, 100000000ull);
-        }
-        __syncthreads();
-    } else if (a.final_state) {
-        float4 *dst = reinterpret_cast<float4 *>(a.final_state + sbase + size_t(tid) * kHeadDim + e0);
+        if (!s.abort && a.final_state) {
+            float4 *dst = reinterpret_cast<float4 *>(a.final_state + sbase + size_t(t) * kHeadDim + e0);
 #pragma unroll
-        for (int q = 0; q < 16; ++q) dst[q] = make_float4(Sr[4 * q], Sr[4 * q + 1], Sr[4 * q + 2], Sr[4 * q + 3]);
+            for (int q = 0; q < 16; ++q) dst[q] = make_float4(Sr[4 * q], Sr[4 * q + 1], Sr[4 * q + 2], Sr[4 * q + 3]);
+        }
+    }
+    __syncthreads();
+    if (s.abort) {
+        if (tid == 0) record_status(a.status, GDN_ETIMEOUT);
+        if (tid == kMathThreads) {  // bounded drain of copies that may be in flight
+            mbar_wait(&s.full[0], 0, 100000000ull);
+            mbar_wait(&s.full[1], 0, 100000000ull);
+        }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 512);
+    if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
 }  // namespace
 
 size_t prefill_tc_workspace(int max_chunks, int hv) {
     const size_t units = size_t(max_chunks) * hv;
-    return al256(units * kTile64) + al256(units * 128 * sizeof(float));
+    return al256(units * kUnitBytes) + al256(units * 128 * sizeof(float));
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs &a, void *ws_data, cudaStream_t s) {
@@ -585,13 +705,13 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, void *ws_data, cudaStream_t 
         return e;
     if (a.max_chunks > 0 && T > 0) {
         LaunchScope scope(GDN_K_CHUNK_PREPARE_TC, s);
-        k_chunk_prepare_tc<<<dim3(a.max_chunks, a.hq), kTcThreads, prep_smem, s>>>(a, w, tk);
+        k_chunk_prepare_tc<<<dim3(a.max_chunks, a.hq), kPrepThreads, prep_smem, s>>>(a, w, tq, tk);
     }
     if ((e = cudaGetLastError())) return e;
     {
         LaunchScope scope(GDN_K_STATE_OUTPUT_TC, s);
         StateArgs sa{a, w};
-        k_chunk_state_output_tc<<<dim3(2 * a.num_seqs, a.hv), kTcThreads, state_smem, s>>>(sa, tq, tk, tv);
+        k_chunk_state_output_tc<<<dim3(2 * a.num_seqs, a.hv), kStateThreads, state_smem, s>>>(sa, tq, tk, tv);
     }
     return cudaGetLastError();
 }

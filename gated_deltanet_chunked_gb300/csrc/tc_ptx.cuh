@@ -164,7 +164,7 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 }
 
 // 32 lanes x 32 bits, 16 consecutive columns per thread.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
     uint32_t r[16];
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
