@@ -418,7 +418,7 @@ struct StateSmem {
     alignas(1024) uint8_t Sb[2 * kTile];  // S_c bf16 [d][e] (128 rows), MN-major B
     alignas(1024) uint8_t Vp[kTile];      // V'_c bf16 [i][e], MN-major B
     alignas(1024) uint8_t Vd[kTile];      // diag(d_c) V'_c bf16 [i][e], MN-major B
-    uint64_t full[2], empty[2], ready, mma;
+    uint64_t full[2], empty[2], ready, mma_s, mma;
     uint32_t tmem;
     int abort;
 };
@@ -431,6 +431,7 @@ struct StateArgs {
 // dynamic shared memory per block is capped at 227 KiB; one more KiB is
 // requested to align the base to 1024 bytes
 static_assert(sizeof(StateSmem) + 1024 <= 227 * 1024, "state kernel shared memory");
+static_assert(sizeof(StepBuf) % 1024 == 0, "step buffers keep the 1024-byte swizzle alignment");
 static_assert(2 * (sizeof(PrepSmem) + 1024) <= 228 * 1024, "two prepare CTAs per SM");
 
 __global__ void __launch_bounds__(kStateThreads, 1)
@@ -460,6 +461,7 @@ k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
             mbar_init(&s.empty[b], 1);
         }
         mbar_init(&s.ready, kMathThreads);
+        mbar_init(&s.mma_s, 1);
         mbar_init(&s.mma, 1);
         fence_mbar_init();
     }
@@ -511,24 +513,24 @@ k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
                 mbar_arrive_expect_tx(&s.full[b], bytes);
                 if (cur) {
                     const int cg = si.first_chunk + c;
-                    const ChunkInfo ci = a.chunk_info[cg];
+                    const int start = si.start + kChunk * c;
                     const uint8_t *uo = w.unit + (size_t(cg) * a.hv + h) * kUnitBytes;
                     for (int hf = 0; hf < 2; ++hf) {
-                        tma_load_3d(B.A1 + hf * 2 * kTile + kTile, &tm_q, 64 * hf, hk, ci.start, &s.full[b]);
-                        tma_load_3d(B.Kt + hf * kTile, &tm_k, 64 * hf, hk, ci.start, &s.full[b]);
+                        tma_load_3d(B.A1 + hf * 2 * kTile + kTile, &tm_q, 64 * hf, hk, start, &s.full[b]);
+                        tma_load_3d(B.Kt + hf * kTile, &tm_k, 64 * hf, hk, start, &s.full[b]);
                     }
                     bulk_load(B.A2 + kTile, uo + kUnitP, kTile, &s.full[b]);
                     bulk_load(B.gbc, w.gb + (size_t(cg) * a.hv + h) * 128, 512, &s.full[b]);
                 }
                 if (nxt) {
                     const int cg = si.first_chunk + c + 1;
-                    const ChunkInfo ci = a.chunk_info[cg];
+                    const int start = si.start + kChunk * (c + 1);
                     const uint8_t *uo = w.unit + (size_t(cg) * a.hv + h) * kUnitBytes;
                     bulk_load(B.A0, uo + kUnitAb, kTile, &s.full[b]);
                     bulk_load(B.A1, uo + kUnitW, kTile, &s.full[b]);
                     bulk_load(B.A1 + 2 * kTile, uo + kUnitW + kTile, kTile, &s.full[b]);
                     bulk_load(B.A2, uo + kUnitG, kTile, &s.full[b]);
-                    tma_load_3d(B.Bv, &tm_v, e0, h, ci.start, &s.full[b]);
+                    tma_load_3d(B.Bv, &tm_v, e0, h, start, &s.full[b]);
                     bulk_load(B.gbn, w.gb + (size_t(cg) * a.hv + h) * 128, 512, &s.full[b]);
                 }
             }
@@ -538,7 +540,18 @@ k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
         if (lane == 0 && nc > 0) {
             const uint32_t id_kmn = idesc_bf16_f32(128, 64, false, true);
             const uint32_t id_mnmn = idesc_bf16_f32(128, 64, true, true);
-            const uint32_t sb = smem_u32(s.Sb), vp = smem_u32(s.Vp), vd = smem_u32(s.Vd);
+            // descriptors of every operand base; a K step only adds its byte
+            // offset >> 4 to the start-address field (no carry: < 256 KiB)
+            const uint64_t dS = sdesc_sw128(smem_u32(s.Sb), kTile, 1024);
+            const uint64_t dVp = sdesc_sw128(smem_u32(s.Vp), kTile, 1024);
+            const uint64_t dVd = sdesc_sw128(smem_u32(s.Vd), kTile, 1024);
+            // the two step buffers differ by a constant byte offset
+            const uint64_t dA0_0 = sdesc_sw128(smem_u32(s.buf[0].A0), 16, 1024);
+            const uint64_t dA1_0 = sdesc_sw128(smem_u32(s.buf[0].A1), 16, 1024);
+            const uint64_t dA2_0 = sdesc_sw128(smem_u32(s.buf[0].A2), 16, 1024);
+            const uint64_t dBv_0 = sdesc_sw128(smem_u32(s.buf[0].Bv), kTile, 1024);
+            const uint64_t dKt_0 = sdesc_sw128(smem_u32(s.buf[0].Kt), kTile, 1024);
+            const uint64_t dbuf = uint64_t(sizeof(StepBuf) >> 4);
             for (int c = -1; c < nc && !s.abort; ++c) {
                 const int b = (c + 1) & 1;
                 if (!mbar_wait(&s.ready, (c + 1) & 1)) {
@@ -546,25 +559,23 @@ k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
                     break;
                 }
                 tc_fence_after();
-                StepBuf &B = s.buf[b];
-                const uint32_t a0 = smem_u32(B.A0), a1 = smem_u32(B.A1), a2 = smem_u32(B.A2);
-                const uint32_t bv = smem_u32(B.Bv), kt = smem_u32(B.Kt);
+                const uint64_t ob = b ? dbuf : 0;
+                const uint64_t dA0 = dA0_0 + ob, dA1 = dA1_0 + ob, dA2 = dA2_0 + ob, dBv = dBv_0 + ob,
+                               dKt = dKt_0 + ob;
+#pragma unroll
+                for (int t = 0; t < 4; ++t)  // D2 = K_c^T diag(d_c) V'_c (state update first)
+                    mma_bf16(tmem + kTmD2, dKt + (2048 * t >> 4), dVd + (2048 * t >> 4), id_mnmn, t > 0);
+                mma_commit(&s.mma_s);
 #pragma unroll
                 for (int t = 0; t < 4; ++t)  // [A B ; 0] V_{c+1}
-                    mma_bf16(tmem + kTmD1, sdesc_sw128(a0 + 32 * t, 16, 1024), sdesc_sw128(bv + 2048 * t, kTile, 1024),
-                             id_kmn, t > 0);
+                    mma_bf16(tmem + kTmD1, dA0 + (32 * t >> 4), dBv + (2048 * t >> 4), id_kmn, t > 0);
 #pragma unroll
                 for (int t = 0; t < 8; ++t)  // [-W' ; Gamma Q] S_c
-                    mma_bf16(tmem + kTmD1, sdesc_sw128(a1 + (t >> 2) * 2 * kTile + (t & 3) * 32, 16, 1024),
-                             sdesc_sw128(sb + 2048 * t, kTile, 1024), id_kmn, 1);
+                    mma_bf16(tmem + kTmD1, dA1 + (((t >> 2) * 2 * kTile + (t & 3) * 32) >> 4),
+                             dS + (2048 * t >> 4), id_kmn, 1);
 #pragma unroll
                 for (int t = 0; t < 4; ++t)  // [-G ; P] V'_c
-                    mma_bf16(tmem + kTmD1, sdesc_sw128(a2 + 32 * t, 16, 1024), sdesc_sw128(vp + 2048 * t, kTile, 1024),
-                             id_kmn, 1);
-#pragma unroll
-                for (int t = 0; t < 4; ++t)  // K_c^T diag(d_c) V'_c
-                    mma_bf16(tmem + kTmD2, sdesc_sw128(kt + 2048 * t, kTile, 1024),
-                             sdesc_sw128(vd + 2048 * t, kTile, 1024), id_mnmn, t > 0);
+                    mma_bf16(tmem + kTmD1, dA2 + (32 * t >> 4), dVp + (2048 * t >> 4), id_kmn, 1);
                 mma_commit(&s.mma);
                 mma_commit(&s.empty[b]);
             }
@@ -572,52 +583,76 @@ k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
     } else {
         // --------------------------- math warps ----------------------------
         const int t = tid;  // TMEM lane and state row
+        const int last_len = si.len - kChunk * (nc - 1);  // valid length of the last chunk
+        // Gamma_c Q_c in place (rows 64..127 of A1 of the step's buffer)
+        auto scale_q = [&](StepBuf &B) {
+#pragma unroll
+            for (int k2 = 0; k2 < 8; ++k2) {
+                const int p = t + kMathThreads * k2;  // 1024 chunks: 64 rows x 16
+                const int r = p >> 4, hf = (p >> 3) & 1, ch = p & 7;
+                uint8_t *ptr = B.A1 + hf * 2 * kTile + kTile + sw128_offset(r, ch);
+                float x[8];
+                unpack8(*reinterpret_cast<const uint4 *>(ptr), x);
+                const float gr = __expf(B.gbc[r]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] *= gr;
+                *reinterpret_cast<uint4 *>(ptr) = pack8(x);
+            }
+        };
+        auto len_of = [&](int c) { return c == nc - 1 ? last_len : kChunk; };
+        // A step buffer is handed back to the producer as soon as the step's
+        // MMAs complete, so every value the epilogue needs from it (gamma_c,
+        // d_{c+1}) is read into registers while the buffer is known to hold
+        // this step's data: one step ahead, right after its copies land.
+        float gam_cur = 1.f, dn_cur = 0.f;  // gamma_c and d_{c+1}[t] of the current step
+        if (nc > 0) {
+            if (!mbar_wait(&s.full[0], 0)) s.abort = 1;  // step -1 reads buffer 0 (no Q)
+            const int l0 = len_of(0);
+            dn_cur = t < l0 ? __expf(s.buf[0].gbn[l0 - 1] - s.buf[0].gbn[t]) : 0.f;
+        }
         // an empty sequence has no steps at all (not even the virtual c = -1):
         // its final state is its initial state
         for (int c = -1; nc > 0 && c < nc && !s.abort; ++c) {
-            const int b = (c + 1) & 1, use = (c + 1) >> 1;
-            StepBuf &B = s.buf[b];
-            if (!mbar_wait(&s.full[b], use & 1)) {
-                s.abort = 1;
-                break;
-            }
-            // Gamma_c Q_c in place (rows 64..127 of A1), then hand over
-            if (c >= 0) {
-#pragma unroll
-                for (int k2 = 0; k2 < 8; ++k2) {
-                    const int p = t + kMathThreads * k2;  // 1024 chunks: 64 rows x 16
-                    const int r = p >> 4, hf = (p >> 3) & 1, ch = p & 7;
-                    uint8_t *ptr = B.A1 + hf * 2 * kTile + kTile + sw128_offset(r, ch);
-                    float x[8];
-                    unpack8(*reinterpret_cast<const uint4 *>(ptr), x);
-                    const float gr = __expf(B.gbc[r]);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] *= gr;
-                    *reinterpret_cast<uint4 *>(ptr) = pack8(x);
-                }
-            }
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&s.ready);
+            // next step's buffer: wait for its copies, scale its Q, take its gates
+            float gam_nxt = 1.f, dn_nxt = 0.f;
+            if (c + 1 < nc) {
+                const int bn = (c + 2) & 1, usen = (c + 2) >> 1;
+                if (!mbar_wait(&s.full[bn], usen & 1)) {
+                    s.abort = 1;
+                    break;
+                }
+                StepBuf &N = s.buf[bn];
+                scale_q(N);
+                gam_nxt = __expf(N.gbc[len_of(c + 1) - 1]);
+                if (c + 2 < nc) {
+                    const int l2 = len_of(c + 2);
+                    dn_nxt = t < l2 ? __expf(N.gbn[l2 - 1] - N.gbn[t]) : 0.f;
+                }
+            }
+            const int lc = c < 0 ? 0 : len_of(c);
+            // state update: S_{c+1}[t] = gamma_c S_c[t] + D2[t]
+            if (!mbar_wait(&s.mma_s, (c + 1) & 1)) {
+                s.abort = 1;
+                break;
+            }
+            tc_fence_after();
+            {
+                float v[64];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) tmem_ld16(tmem_addr(tmem, 32 * warp, kTmD2 + 16 * j), v + 16 * j);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 64; ++e) Sr[e] = fmaf(gam_cur, Sr[e], v[e]);
+            }
+            // D1 rows: V'_{c+1} (t < 64) or O_c (t >= 64)
             if (!mbar_wait(&s.mma, (c + 1) & 1)) {
                 s.abort = 1;
                 break;
             }
             tc_fence_after();
-            // state update: S_{c+1}[t] = gamma_c S_c[t] + D2[t]
-            {
-                const int lc = c >= 0 ? a.chunk_info[si.first_chunk + c].len : 0;
-                const float gam = c >= 0 ? __expf(B.gbc[lc - 1]) : 1.f;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    float v[16];
-                    tmem_ld16(tmem_addr(tmem, 32 * warp, kTmD2 + 16 * j), v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) Sr[16 * j + e] = fmaf(gam, Sr[16 * j + e], v[e]);
-                }
-            }
-            // D1 rows: V'_{c+1} (t < 64) or O_c (t >= 64)
             float d1[64];
 #pragma unroll
             for (int j = 0; j < 4; ++j) tmem_ld16(tmem_addr(tmem, 32 * warp, kTmD1 + 16 * j), d1 + 16 * j);
@@ -628,23 +663,20 @@ k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
                 *reinterpret_cast<uint4 *>(s.Sb + sw128_offset(t, ch)) = pack8(Sr + 8 * ch);
             if (t < 64) {
                 if (c + 1 < nc) {
-                    const int ln = a.chunk_info[si.first_chunk + c + 1].len;
-                    const float dn = t < ln ? __expf(B.gbn[ln - 1] - B.gbn[t]) : 0.f;
                     float vd[8];
 #pragma unroll
                     for (int ch = 0; ch < 8; ++ch) {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) vd[e] = dn * d1[8 * ch + e];
+                        for (int e = 0; e < 8; ++e) vd[e] = dn_cur * d1[8 * ch + e];
                         *reinterpret_cast<uint4 *>(s.Vp + sw128_offset(t, ch)) = pack8(d1 + 8 * ch);
                         *reinterpret_cast<uint4 *>(s.Vd + sw128_offset(t, ch)) = pack8(vd);
                     }
                 }
             } else if (c >= 0) {
                 const int r = t - 64;
-                const ChunkInfo ci = a.chunk_info[si.first_chunk + c];
-                if (r < ci.len) {
-                    __nv_bfloat16 *orow =
-                        static_cast<__nv_bfloat16 *>(a.out) + (size_t(ci.start + r) * a.hv + h) * kHeadDim + e0;
+                if (r < lc) {
+                    __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) +
+                                          (size_t(si.start + kChunk * c + r) * a.hv + h) * kHeadDim + e0;
                     float o[8];
 #pragma unroll
                     for (int ch = 0; ch < 8; ++ch) {
@@ -654,6 +686,8 @@ k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
                     }
                 }
             }
+            gam_cur = gam_nxt;
+            dn_cur = dn_nxt;
         }
         if (!s.abort && a.final_state) {
             float4 *dst = reinterpret_cast<float4 *>(a.final_state + sbase + size_t(t) * kHeadDim + e0);
