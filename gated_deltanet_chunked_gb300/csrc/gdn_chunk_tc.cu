@@ -18,11 +18,11 @@
 // M = 128 MMAs (an M = 64 MMA runs at half the rate):
 //   D1 = [A_c+1 B ; 0] V_{c+1} + [-gamma_c W_{c+1} ; Gamma_c Q_c] S_c
 //        + [-G_c ; P_c] V'_c         rows 0..63 = V'_{c+1}, rows 64..127 = O_c/scale
-//   D2 = K_c^T (diag(d_c) V'_c)      S_{c+1} = gamma_c S_c + D2
+//   D2 = (diag(d_c) K_c)^T V'_c      S_{c+1} = gamma_c S_c + D2
 // The walk starts at a virtual step c = -1 with S_-1 = S0, V'_-1 = 0,
 // gamma_-1 = 1 and G_-1 = 0, which yields V'_0 = U_0 - W_0 S0.
 //
-// k_chunk_prepare_tc (grid: chunk x q/k head, all SMs): gate prefix sums,
+// k_chunk_prepare_tc (grid: chunk x v-head, all SMs): gate prefix sums,
 //   [K;Q] K^T in one M=128 MMA, the masked gated M and its unit-lower-
 //   triangular inverse by blocked (16x16) forward substitution in f32, then
 //   W_c and G_{c-1} on the tensor cores. Writes, per (chunk, v-head), bf16
@@ -114,36 +114,49 @@ __device__ __forceinline__ void warp_scan64(float &a0, float &a1, int lane) {
 }
 
 // ===========================================================================
-// k_chunk_prepare_tc
+// k_chunk_prepare_tc: one CTA per (chunk, v-head), 128 threads, 3 CTAs/SM
 // ===========================================================================
-constexpr int kPrepThreads = 256;
+constexpr int kPrepThreads = 128;
 
 struct PrepSmem {
-    alignas(1024) uint8_t KQ[4 * kTile];  // [K_c ; Q_c] K-major, M = 128: two d-halves of 16 KiB
+    alignas(1024) uint8_t KQ[4 * kTile];  // [K_c ; Q_c] K-major, M = 128 (two d-halves of 16 KiB)
     alignas(1024) uint8_t Kp[2 * kTile];  // K_{c-1}, two d-halves
-    alignas(1024) uint8_t Ag[kTile];      // A diag(beta gamma) bf16 [i][j]
-    alignas(1024) uint8_t Wb[2 * kTile];  // W_c bf16 [i][d]
-    float M[64 * kFPitch];                // strict lower gated K K^T
-    float X[64 * kFPitch];                // (I + M)^-1
-    float T[3 * 256];                     // block products of the solve
-    float gc[64], beta[64], gcp[64], dprev[64];
+    // A diag(beta gamma) bf16 [i][j]; before the solve ends it holds the raw
+    // gates (g, gp) and the 16x16 block product T of the solve
+    alignas(1024) uint8_t Ag[kTile];
+    alignas(1024) float MX[64 * kFPitch]; // M, inverted in place into A; later W_c bf16 [i][d]
+    float beta[64], gc[64], gcp[64];
     uint64_t bar_load, bar_mma;
     uint32_t tmem;
     int abort;
 };
 
-__global__ void __launch_bounds__(kPrepThreads, 2)
+// MX (17 KiB) must also hold the bf16 W tile (16 KiB) once the solve is done
+static_assert(64 * kFPitch * sizeof(float) >= 2 * kTile, "W tile reuses the solve buffer");
+
+__global__ void __launch_bounds__(kPrepThreads, 3)
 k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k) {
     extern __shared__ uint8_t smraw[];
     PrepSmem &s = *reinterpret_cast<PrepSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
-    const int c = blockIdx.x, hk = blockIdx.y;
+    const int c = blockIdx.x, h = blockIdx.y, hk = h / a.group;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (c >= *a.n_chunks) return;  // also a rejected chunk table (-1)
     const ChunkInfo ci = a.chunk_info[c];
     const int l = ci.len;
-    const bool has_prev = ci.idx > 0;
+    const bool has_prev = ci.idx > 0;  // chunk c-1 belongs to the same sequence (and is full)
     const int prev_start = ci.start - kChunk;
+    const size_t unit = size_t(c) * a.hv + h;
+    uint8_t *uo = w.unit + unit * kUnitBytes;
+    float *M = s.MX;
+    // scratch in the Ag region, all consumed before Ag is written
+    float *graw = reinterpret_cast<float *>(s.Ag);  // [64] gates of chunk c
+    float *gpraw = graw + 64;                       // [64] gates of chunk c-1
+    float *T = graw + 128;                          // [256] block product of the solve
+    float *colf = graw + 384;                       // [64]  exp(gc_{e(j)} - gc_j)
+    float *rowf = graw + 448;                       // [64][4] exp(gc_i - gc_{e(b)}), b < i/16
+    float *DB = graw + 704;                         // [4][16][17] exp(gc_r - gc_i) within a block
+    constexpr int kDBp = 17;                        // padded row: lanes of a warp hit distinct banks
 
     if (tid == 0) {
         s.abort = 0;
@@ -157,15 +170,23 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
             if (has_prev) tma_load_3d(s.Kp + hf * kTile, &tm_k, 64 * hf, hk, prev_start, &s.bar_load);
         }
     }
+    // gates of this chunk and of the previous one (independent loads, issued
+    // before anything waits)
+    if (tid < 64) {
+        graw[tid] = tid < l ? a.g[size_t(ci.start + tid) * a.hv + h] : 0.f;
+        gpraw[tid] = has_prev ? a.g[size_t(prev_start + tid) * a.hv + h] : 0.f;
+    } else {
+        const int i = tid - 64;
+        s.beta[i] = i < l ? a.beta[size_t(ci.start + i) * a.hv + h] : 0.f;
+    }
     if (warp == 0) {
-        tmem_alloc(&s.tmem, 256);
+        tmem_alloc(&s.tmem, 128);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s.tmem;
-    const uint32_t kTmKK = 0, kTmW = 64, kTmG = 192;
     uint32_t mma_phase = 0;
 
     // [K;Q] K^T : M=128 (rows 0-63 K K^T, rows 64-127 Q K^T), N=64, K=128
@@ -177,215 +198,256 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
                 const uint32_t off = (t >> 2) * 2 * kTile + (t & 3) * 32;
-                mma_bf16(tmem + kTmKK, sdesc_sw128(kq + off, 16, 1024), sdesc_sw128(kq + off, 16, 1024), id, t > 0);
+                mma_bf16(tmem, sdesc_sw128(kq + off, 16, 1024), sdesc_sw128(kq + off, 16, 1024), id, t > 0);
             }
             mma_commit(&s.bar_mma);
         } else {
             s.abort = 1;
         }
     }
+    // gate prefix sums while the MMA runs (warp 0: chunk c, warp 1: chunk c-1)
+    float gprev = -1.f;  // -gamma_{c-1} (1 for the first chunk of a sequence)
+    if (warp < 2) {
+        const float *src = warp == 0 ? graw : gpraw;
+        float a0 = src[2 * lane], a1 = src[2 * lane + 1];
+        warp_scan64(a0, a1, lane);
+        float *dst = warp == 0 ? s.gc : s.gcp;
+        dst[2 * lane] = a0;
+        dst[2 * lane + 1] = a1;
+    }
+    __syncthreads();
+    const float gp63 = s.gcp[63];  // read before gcp is overwritten with d_{c-1}
+    if (has_prev) gprev = -__expf(gp63);
+    __syncthreads();
+    // Decay factors exp(gc_r - gc_i), i <= r, from about 1.5K exponentials
+    // instead of one per matrix entry. Within a 16-row block they are taken
+    // directly; across blocks, with e(b) = 16 b + 15 the last row of block b,
+    //   exp(gc_r - gc_i) = exp(gc_r - gc_e(b_i)) * exp(gc_e(b_i) - gc_i),
+    // where both factors are <= 1 because the gates are log-decays (g <= 0,
+    // so gc does not increase along the chunk). gamma_j = exp(gc_j) and
+    // d_{c-1,i'} = exp(gc_{c-1,63} - gc_{c-1,i'}) are tabulated the same way.
+    if (tid < 64) {
+        w.gb[unit * 128 + tid] = s.gc[tid];
+        w.gb[unit * 128 + 64 + tid] = s.beta[tid];
+        colf[tid] = __expf(s.gc[16 * (tid >> 4) + 15] - s.gc[tid]);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) rowf[4 * tid + b] = b < (tid >> 4) ? __expf(s.gc[tid] - s.gc[16 * b + 15]) : 0.f;
+    } else {
+        const int j = tid - 64;
+        s.gcp[j] = has_prev ? __expf(gp63 - s.gcp[j]) : 0.f;  // becomes d_{c-1}
+    }
+    for (int e = tid; e < 1024; e += kPrepThreads) {
+        const int b = e >> 8, r = (e >> 4) & 15, i = e & 15;
+        DB[(b * 16 + r) * kDBp + i] = i <= r ? __expf(s.gc[16 * b + r] - s.gc[16 * b + i]) : 0.f;
+    }
+    if (!s.abort && !mbar_wait(&s.bar_mma, mma_phase)) s.abort = 1;
+    mma_phase ^= 1;
+    tc_fence_after();
+    // ---- M (rows 0-63: K K^T) and P (rows 64-127: Q K^T), one row per thread ----
+    if (!s.abort) {
+        float v[64];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) tmem_ld16(tmem_addr(tmem, 32 * warp, 16 * j), v + 16 * j);
+        tmem_ld_wait();
+        const int r = tid & 63, br = r >> 4;  // row (of M or P) and its 16-block
+        const float *db = DB + (br * 16 + (r & 15)) * kDBp;
+        float rf[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) rf[b] = rowf[4 * r + b];
+        // decay factor of column i for row r (i <= r), 0 otherwise
+        auto decay = [&](int i) {
+            const int bi = i >> 4;
+            return bi == br ? db[i & 15] : (bi < br ? rf[bi] * colf[i] : 0.f);
+        };
+        if (warp < 2) {
+            const float bi = s.beta[r];
+#pragma unroll
+            for (int j = 0; j < 64; ++j) v[j] = (j < r && r < l) ? bi * decay(j) * v[j] : 0.f;
+            float4 *row = reinterpret_cast<float4 *>(M + r * kFPitch);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) row[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) v[i] = (i <= r && r < l) ? decay(i) * v[i] : 0.f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<uint4 *>(uo + kUnitP + sw128_offset(r, q)) = pack8(v + 8 * q);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tid < 64) s.gc[tid] = __expf(s.gc[tid]);  // gc -> gamma (read only by the A diag(beta gamma) step)
+    // ---- A = (I + M)^-1 in place, 16x16 blocks ----
+
+    // diagonal blocks: thread = (block, column); column kept in registers
+    if (tid < 64) {
+        const int b = tid >> 4, jj = tid & 15;
+        float x[16];
+#pragma unroll
+        for (int ii = 0; ii < 16; ++ii) {
+            float acc = (ii == jj) ? 1.f : 0.f;
+            const float4 *Mr = reinterpret_cast<const float4 *>(M + (16 * b + ii) * kFPitch + 16 * b);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (4 * q < ii) {
+                    const float4 m = Mr[q];
+                    if (4 * q + 0 < ii) acc = fmaf(-m.x, x[4 * q + 0], acc);
+                    if (4 * q + 1 < ii) acc = fmaf(-m.y, x[4 * q + 1], acc);
+                    if (4 * q + 2 < ii) acc = fmaf(-m.z, x[4 * q + 2], acc);
+                    if (4 * q + 3 < ii) acc = fmaf(-m.w, x[4 * q + 3], acc);
+                }
+            }
+            x[ii] = acc;
+        }
+        __syncwarp();
+        // every thread of a block has read the block's M rows before any writes
+        // (the 16 threads of a block sit in the same warp)
+#pragma unroll
+        for (int ii = 0; ii < 16; ++ii) M[(16 * b + ii) * kFPitch + 16 * b + jj] = x[ii];
+    }
+    __syncthreads();
+    // off-diagonal blocks, column block j left to right, rows i = j+1..3:
+
+    //   X_ij = -X_ii sum_{k=j}^{i-1} L_ik X_kj; L_ij is overwritten by X_ij,
+    //   which is safe because later blocks only read L_ik with k > j
+    {
+        const int ii = tid >> 3, jj = 2 * (tid & 7);  // two adjacent outputs per thread
+#pragma unroll 1
+        for (int j = 0; j < 3; ++j) {
+#pragma unroll 1
+            for (int i = j + 1; i < 4; ++i) {
+                float t0 = 0.f, t1 = 0.f;
+                for (int k = j; k < i; ++k) {
+                    const float4 *Lr = reinterpret_cast<const float4 *>(M + (16 * i + ii) * kFPitch + 16 * k);
+                    const float *Xc = M + (16 * k) * kFPitch + 16 * j + jj;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 lq = Lr[q];
+                        const float2 x0 = *reinterpret_cast<const float2 *>(Xc + (4 * q + 0) * kFPitch);
+                        const float2 x1 = *reinterpret_cast<const float2 *>(Xc + (4 * q + 1) * kFPitch);
+                        const float2 x2 = *reinterpret_cast<const float2 *>(Xc + (4 * q + 2) * kFPitch);
+                        const float2 x3 = *reinterpret_cast<const float2 *>(Xc + (4 * q + 3) * kFPitch);
+                        t0 = fmaf(lq.x, x0.x, t0); t1 = fmaf(lq.x, x0.y, t1);
+                        t0 = fmaf(lq.y, x1.x, t0); t1 = fmaf(lq.y, x1.y, t1);
+                        t0 = fmaf(lq.z, x2.x, t0); t1 = fmaf(lq.z, x2.y, t1);
+                        t0 = fmaf(lq.w, x3.x, t0); t1 = fmaf(lq.w, x3.y, t1);
+                    }
+                }
+                T[ii * 16 + jj] = t0;
+                T[ii * 16 + jj + 1] = t1;
+                __syncthreads();
+                const float4 *Xr = reinterpret_cast<const float4 *>(M + (16 * i + ii) * kFPitch + 16 * i);
+                float o0 = 0.f, o1 = 0.f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 xq = Xr[q];  // X_ii row (zero above the diagonal)
+                    const float2 u0 = *reinterpret_cast<const float2 *>(&T[(4 * q + 0) * 16 + jj]);
+                    const float2 u1 = *reinterpret_cast<const float2 *>(&T[(4 * q + 1) * 16 + jj]);
+                    const float2 u2 = *reinterpret_cast<const float2 *>(&T[(4 * q + 2) * 16 + jj]);
+                    const float2 u3 = *reinterpret_cast<const float2 *>(&T[(4 * q + 3) * 16 + jj]);
+                    o0 = fmaf(xq.x, u0.x, o0); o1 = fmaf(xq.x, u0.y, o1);
+                    o0 = fmaf(xq.y, u1.x, o0); o1 = fmaf(xq.y, u1.y, o1);
+                    o0 = fmaf(xq.z, u2.x, o0); o1 = fmaf(xq.z, u2.y, o1);
+                    o0 = fmaf(xq.w, u3.x, o0); o1 = fmaf(xq.w, u3.y, o1);
+                }
+                *reinterpret_cast<float2 *>(M + (16 * i + ii) * kFPitch + 16 * j + jj) = make_float2(-o0, -o1);
+                __syncthreads();
+            }
+        }
+    }
+    // ---- A diag(beta) -> global; A diag(beta gamma) -> smem operand ----
+    // (entries above the diagonal of A are exactly zero: the strictly upper
+    // part of M was never written with anything but zeros)
+    for (int p = tid; p < 512; p += kPrepThreads) {
+        const int i = p >> 3, ch = p & 7;
+        float x[8], y[8];
+        const float4 *xr = reinterpret_cast<const float4 *>(M + i * kFPitch + 8 * ch);
+        const float4 x0 = xr[0], x1 = xr[1];
+        x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
+        x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int j = 8 * ch + e;
+            x[e] = (j <= i) ? x[e] * s.beta[j] : 0.f;
+            y[e] = x[e] * s.gc[j];  // gamma_j
+        }
+        *reinterpret_cast<uint4 *>(uo + kUnitAb + sw128_offset(i, ch)) = pack8(x);
+        *reinterpret_cast<uint4 *>(s.Ag + sw128_offset(i, ch)) = pack8(y);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    // ---- W_c = Ag K_c : M=64, N=128 (d), K=64 (j); K tile read MN-major ----
+    if (tid == 0 && !s.abort) {
+        tc_fence_after();
+        const uint32_t ag = smem_u32(s.Ag), kq = smem_u32(s.KQ);
+        const uint32_t id = idesc_bf16_f32(64, 128, false, true);
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+            mma_bf16(tmem, sdesc_sw128(ag + 32 * t, 16, 1024), sdesc_sw128(kq + 2048 * t, 2 * kTile, 1024), id,
+                     t > 0);
+        mma_commit(&s.bar_mma);
+    }
     __syncthreads();
     if (!s.abort && !mbar_wait(&s.bar_mma, mma_phase)) s.abort = 1;
     mma_phase ^= 1;
-    __syncthreads();
     tc_fence_after();
-
-    const int q4 = warp & 3, colhalf = warp >> 2;
-    for (int hh = 0; !s.abort && hh < a.group; ++hh) {
-        const int h = hk * a.group + hh;
-        const size_t unit = size_t(c) * a.hv + h;
-        uint8_t *uo = w.unit + unit * kUnitBytes;
-        // ---- gate prefix sums (this chunk; previous chunk of the sequence) ----
-        if (warp < 2) {
-            const int base = warp == 0 ? ci.start : prev_start;
-            const int len = warp == 0 ? l : (has_prev ? kChunk : 0);
-            float a0 = 2 * lane < len ? a.g[size_t(base + 2 * lane) * a.hv + h] : 0.f;
-            float a1 = 2 * lane + 1 < len ? a.g[size_t(base + 2 * lane + 1) * a.hv + h] : 0.f;
-            warp_scan64(a0, a1, lane);
-            float *dst = warp == 0 ? s.gc : s.gcp;
-            dst[2 * lane] = a0;
-            dst[2 * lane + 1] = a1;
-        } else if (warp < 4) {
-            const int i = tid - 64;
-            s.beta[i] = i < l ? a.beta[size_t(ci.start + i) * a.hv + h] : 0.f;
-        }
-        __syncthreads();
-        if (tid < 64) {
-            w.gb[unit * 128 + tid] = s.gc[tid];
-            w.gb[unit * 128 + 64 + tid] = s.beta[tid];
-            s.dprev[tid] = has_prev ? __expf(s.gcp[63] - s.gcp[tid]) : 0.f;
-        }
-        // ---- M (from K K^T) and P (from Q K^T), straight out of TMEM ----
-        {
-            float v[32];
-            tmem_ld16(tmem_addr(tmem, 32 * q4, kTmKK + 32 * colhalf), v);
-            tmem_ld16(tmem_addr(tmem, 32 * q4, kTmKK + 32 * colhalf + 16), v + 16);
-            tmem_ld_wait();
-            if (q4 < 2) {
-                const int i = 32 * q4 + lane;
-                const float bi = s.beta[i], gi = s.gc[i];
+    uint8_t *Wb = reinterpret_cast<uint8_t *>(s.MX);  // the solve buffer is free now
+    {
+        const int i = 16 * warp + lane;  // M=64 accumulator row (lanes 0-15)
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int j = 32 * colhalf + e;
-                    s.M[i * kFPitch + j] = (j < i && i < l) ? bi * __expf(gi - s.gc[j]) * v[e] : 0.f;
-                }
-            } else {
-                const int r = 32 * (q4 - 2) + lane;
-                const float gr = s.gc[r];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int i = 32 * colhalf + e;
-                    v[e] = (i <= r && r < l) ? __expf(gr - s.gc[i]) * v[e] : 0.f;
-                }
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    *reinterpret_cast<uint4 *>(uo + kUnitP + sw128_offset(r, 4 * colhalf + q)) = pack8(v + 8 * q);
-            }
-        }
-        __syncthreads();
-        // ---- A = (I + M)^-1, blocked 16x16 forward substitution ----
-        if (tid < 64) {  // diagonal blocks: thread = (block, column)
-            const int b = tid >> 4, jj = tid & 15;
-            float x[16];
-#pragma unroll
-            for (int ii = 0; ii < 16; ++ii) {
-                float acc = (ii == jj) ? 1.f : 0.f;
-                const float *Mr = s.M + (16 * b + ii) * kFPitch + 16 * b;
-#pragma unroll
-                for (int m = 0; m < ii; ++m) acc = fmaf(-Mr[m], x[m], acc);
-                x[ii] = acc;
-            }
-#pragma unroll
-            for (int ii = 0; ii < 16; ++ii) s.X[(16 * b + ii) * kFPitch + 16 * b + jj] = x[ii];
-        } else {  // zero the strictly-upper blocks
-            for (int e = tid - 64; e < 6 * 256; e += kPrepThreads - 64) {
-                const int blk = e >> 8, ii = (e >> 4) & 15, jj = e & 15;
-                const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-                const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-                s.X[(16 * bi + ii) * kFPitch + 16 * bj + jj] = 0.f;
-            }
-        }
-        __syncthreads();
-        {
-            const int ii = tid >> 4, jj = tid & 15;
-#pragma unroll
-            for (int L = 1; L < 4; ++L) {
-                for (int j = 0; j + L < 4; ++j) {  // T = sum_{k=j}^{i-1} M_ik X_kj
-                    const int i = j + L;
-                    float acc = 0.f;
-                    for (int k = j; k < i; ++k) {
-                        const float *Mr = s.M + (16 * i + ii) * kFPitch + 16 * k;
-                        const float *Xc = s.X + (16 * k) * kFPitch + 16 * j + jj;
-#pragma unroll
-                        for (int m = 0; m < 16; ++m) acc = fmaf(Mr[m], Xc[m * kFPitch], acc);
-                    }
-                    s.T[j * 256 + tid] = acc;
-                }
-                __syncthreads();
-                for (int j = 0; j + L < 4; ++j) {  // X_ij = -X_ii T
-                    const int i = j + L;
-                    const float *Xr = s.X + (16 * i + ii) * kFPitch + 16 * i;
-                    float acc = 0.f;
-#pragma unroll
-                    for (int m = 0; m < 16; ++m)
-                        if (m <= ii) acc = fmaf(Xr[m], s.T[j * 256 + m * 16 + jj], acc);
-                    s.X[(16 * i + ii) * kFPitch + 16 * j + jj] = -acc;
-                }
-                __syncthreads();
-            }
-        }
-        // ---- A diag(beta) -> global; A diag(beta gamma) -> smem operand ----
-        for (int p = tid; p < 512; p += kPrepThreads) {
-            const int i = p >> 3, ch = p & 7;
-            float x[8], y[8];
-            const float4 *xr = reinterpret_cast<const float4 *>(s.X + i * kFPitch + 8 * ch);
-            const float4 x0 = xr[0], x1 = xr[1];
-            x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
-            x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int j = 8 * ch + e;
-                x[e] *= s.beta[j];
-                y[e] = x[e] * __expf(s.gc[j]);
-            }
-            *reinterpret_cast<uint4 *>(uo + kUnitAb + sw128_offset(i, ch)) = pack8(x);
-            *reinterpret_cast<uint4 *>(s.Ag + sw128_offset(i, ch)) = pack8(y);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        // ---- W_c = Ag K_c : M=64, N=128 (d), K=64 (j); K tile read MN-major ----
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t ag = smem_u32(s.Ag), kq = smem_u32(s.KQ);
-            const uint32_t id = idesc_bf16_f32(64, 128, false, true);
-#pragma unroll
-            for (int t = 0; t < 4; ++t)
-                mma_bf16(tmem + kTmW, sdesc_sw128(ag + 32 * t, 16, 1024), sdesc_sw128(kq + 2048 * t, 2 * kTile, 1024),
-                         id, t > 0);
-            mma_commit(&s.bar_mma);
-        }
-        if (!mbar_wait(&s.bar_mma, mma_phase)) s.abort = 1;
-        mma_phase ^= 1;
-        tc_fence_after();
-        {
-            const float gprev = has_prev ? -__expf(s.gcp[63]) : -1.f;
-            const int i = 16 * q4 + lane;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float v[16];
-                tmem_ld16(tmem_addr(tmem, 32 * q4, kTmW + 64 * colhalf + 16 * j), v);
-                tmem_ld_wait();
-                if (lane < 16) {
-                    uint8_t *wbh = s.Wb + colhalf * kTile;
-                    uint8_t *woh = uo + kUnitW + colhalf * kTile;
-                    float sv[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) sv[e] = gprev * v[e];
-                    *reinterpret_cast<uint4 *>(wbh + sw128_offset(i, 2 * j)) = pack8(v);
-                    *reinterpret_cast<uint4 *>(wbh + sw128_offset(i, 2 * j + 1)) = pack8(v + 8);
-                    *reinterpret_cast<uint4 *>(woh + sw128_offset(i, 2 * j)) = pack8(sv);
-                    *reinterpret_cast<uint4 *>(woh + sw128_offset(i, 2 * j + 1)) = pack8(sv + 8);
-                }
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        // ---- G_{c-1} = W_c K_{c-1}^T diag(d_{c-1}) : M=64, N=64, K=128 ----
-        if (has_prev) {
-            if (tid == 0) {
-                tc_fence_after();
-                const uint32_t wb = smem_u32(s.Wb), kp = smem_u32(s.Kp);
-                const uint32_t id = idesc_bf16_f32(64, 64, false, false);
-#pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    const uint32_t off = (t >> 2) * kTile + (t & 3) * 32;
-                    mma_bf16(tmem + kTmG, sdesc_sw128(wb + off, 16, 1024), sdesc_sw128(kp + off, 16, 1024), id, t > 0);
-                }
-                mma_commit(&s.bar_mma);
-            }
-            if (!mbar_wait(&s.bar_mma, mma_phase)) s.abort = 1;
-            mma_phase ^= 1;
-            tc_fence_after();
-            const int i = 16 * q4 + lane;
-            float v[32];
-            tmem_ld16(tmem_addr(tmem, 32 * q4, kTmG + 32 * colhalf), v);
-            tmem_ld16(tmem_addr(tmem, 32 * q4, kTmG + 32 * colhalf + 16), v + 16);
+        for (int j = 0; j < 8; ++j) {
+            float v[16];
+            tmem_ld16(tmem_addr(tmem, 32 * warp, 16 * j), v);
             tmem_ld_wait();
             if (lane < 16) {
+                uint8_t *wbh = Wb + (j >> 2) * kTile;
+                uint8_t *woh = uo + kUnitW + (j >> 2) * kTile;
+                float sv[16];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] = -v[e] * s.dprev[32 * colhalf + e];
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    *reinterpret_cast<uint4 *>(uo + kUnitG + sw128_offset(i, 4 * colhalf + q)) = pack8(v + 8 * q);
+                for (int e = 0; e < 16; ++e) sv[e] = gprev * v[e];
+                *reinterpret_cast<uint4 *>(wbh + sw128_offset(i, (2 * j) & 7)) = pack8(v);
+                *reinterpret_cast<uint4 *>(wbh + sw128_offset(i, (2 * j + 1) & 7)) = pack8(v + 8);
+                *reinterpret_cast<uint4 *>(woh + sw128_offset(i, (2 * j) & 7)) = pack8(sv);
+                *reinterpret_cast<uint4 *>(woh + sw128_offset(i, (2 * j + 1) & 7)) = pack8(sv + 8);
             }
-        } else {
-            for (int p = tid; p < int(kTile / 16); p += kPrepThreads)
-                reinterpret_cast<uint4 *>(uo + kUnitG)[p] = make_uint4(0, 0, 0, 0);
         }
-        tc_fence_before();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    // ---- G_{c-1} = W_c K_{c-1}^T diag(d_{c-1}) : M=64, N=64, K=128 ----
+    if (has_prev) {
+        if (tid == 0 && !s.abort) {
+            tc_fence_after();
+            const uint32_t wb = smem_u32(Wb), kp = smem_u32(s.Kp);
+            const uint32_t id = idesc_bf16_f32(64, 64, false, false);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const uint32_t off = (t >> 2) * kTile + (t & 3) * 32;
+                mma_bf16(tmem, sdesc_sw128(wb + off, 16, 1024), sdesc_sw128(kp + off, 16, 1024), id, t > 0);
+            }
+            mma_commit(&s.bar_mma);
+        }
         __syncthreads();
+        if (!s.abort && !mbar_wait(&s.bar_mma, mma_phase)) s.abort = 1;
+        mma_phase ^= 1;
+        tc_fence_after();
+        const int i = 16 * warp + lane;
+        float v[64];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) tmem_ld16(tmem_addr(tmem, 32 * warp, 16 * j), v + 16 * j);
+        tmem_ld_wait();
+        if (lane < 16) {
+#pragma unroll
+            for (int e = 0; e < 64; ++e) v[e] = -v[e] * s.gcp[e];  // d_{c-1}
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<uint4 *>(uo + kUnitG + sw128_offset(i, q)) = pack8(v + 8 * q);
+        }
+    } else {
+        for (int p = tid; p < int(kTile / 16); p += kPrepThreads)
+            reinterpret_cast<uint4 *>(uo + kUnitG)[p] = make_uint4(0, 0, 0, 0);
     }
     if (s.abort && tid == 0) {
         record_status(a.status, GDN_ETIMEOUT);
@@ -393,7 +455,7 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
 // ===========================================================================
@@ -408,16 +470,14 @@ struct StepBuf {
     alignas(1024) uint8_t A1[4 * kTile];  // [-W'_{c+1} ; Gamma_c Q_c] K-major, M=128, K=128 (two d-halves)
     alignas(1024) uint8_t A2[2 * kTile];  // [-G_c ; P_c]             K-major, M=128, K=64
     alignas(1024) uint8_t Bv[kTile];      // V_{c+1}[:, tile]         MN-major B, [j][e]
-    alignas(1024) uint8_t Kt[2 * kTile];  // K_c                      MN-major A (K^T), [i][d]
+    alignas(1024) uint8_t Kt[2 * kTile];  // diag(d_c) K_c             MN-major A (K^T), [i][d]
     float gbc[128];                       // gc, beta of chunk c
-    float gbn[128];                       // gc, beta of chunk c+1
 };
 
 struct StateSmem {
     StepBuf buf[2];
     alignas(1024) uint8_t Sb[2 * kTile];  // S_c bf16 [d][e] (128 rows), MN-major B
     alignas(1024) uint8_t Vp[kTile];      // V'_c bf16 [i][e], MN-major B
-    alignas(1024) uint8_t Vd[kTile];      // diag(d_c) V'_c bf16 [i][e], MN-major B
     uint64_t full[2], empty[2], ready, mma_s, mma;
     uint32_t tmem;
     int abort;
@@ -432,7 +492,8 @@ struct StateArgs {
 // requested to align the base to 1024 bytes
 static_assert(sizeof(StateSmem) + 1024 <= 227 * 1024, "state kernel shared memory");
 static_assert(sizeof(StepBuf) % 1024 == 0, "step buffers keep the 1024-byte swizzle alignment");
-static_assert(2 * (sizeof(PrepSmem) + 1024) <= 228 * 1024, "two prepare CTAs per SM");
+// three CTAs per SM: 228 KiB per SM, 1 KiB reserved per CTA, 1 KiB alignment slack
+static_assert(3 * (sizeof(PrepSmem) + 2048) <= 228 * 1024, "three prepare CTAs per SM");
 
 __global__ void __launch_bounds__(kStateThreads, 1)
 k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
@@ -509,7 +570,7 @@ k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
                 uint32_t bytes = 0;
                 const bool cur = c >= 0, nxt = c + 1 < nc;
                 if (cur) bytes += 2 * kTile /*Q*/ + kTile /*P*/ + 2 * kTile /*K*/ + 512;
-                if (nxt) bytes += kTile /*Ab*/ + 2 * kTile /*W*/ + kTile /*G*/ + kTile /*V*/ + 512;
+                if (nxt) bytes += kTile /*Ab*/ + 2 * kTile /*W*/ + kTile /*G*/ + kTile /*V*/;
                 mbar_arrive_expect_tx(&s.full[b], bytes);
                 if (cur) {
                     const int cg = si.first_chunk + c;
@@ -531,7 +592,6 @@ k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
                     bulk_load(B.A1 + 2 * kTile, uo + kUnitW + kTile, kTile, &s.full[b]);
                     bulk_load(B.A2, uo + kUnitG, kTile, &s.full[b]);
                     tma_load_3d(B.Bv, &tm_v, e0, h, start, &s.full[b]);
-                    bulk_load(B.gbn, w.gb + (size_t(cg) * a.hv + h) * 128, 512, &s.full[b]);
                 }
             }
         }
@@ -544,7 +604,6 @@ k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
             // offset >> 4 to the start-address field (no carry: < 256 KiB)
             const uint64_t dS = sdesc_sw128(smem_u32(s.Sb), kTile, 1024);
             const uint64_t dVp = sdesc_sw128(smem_u32(s.Vp), kTile, 1024);
-            const uint64_t dVd = sdesc_sw128(smem_u32(s.Vd), kTile, 1024);
             // the two step buffers differ by a constant byte offset
             const uint64_t dA0_0 = sdesc_sw128(smem_u32(s.buf[0].A0), 16, 1024);
             const uint64_t dA1_0 = sdesc_sw128(smem_u32(s.buf[0].A1), 16, 1024);
@@ -563,8 +622,8 @@ k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
                 const uint64_t dA0 = dA0_0 + ob, dA1 = dA1_0 + ob, dA2 = dA2_0 + ob, dBv = dBv_0 + ob,
                                dKt = dKt_0 + ob;
 #pragma unroll
-                for (int t = 0; t < 4; ++t)  // D2 = K_c^T diag(d_c) V'_c (state update first)
-                    mma_bf16(tmem + kTmD2, dKt + (2048 * t >> 4), dVd + (2048 * t >> 4), id_mnmn, t > 0);
+                for (int t = 0; t < 4; ++t)  // D2 = (diag(d_c) K_c)^T V'_c (state update first)
+                    mma_bf16(tmem + kTmD2, dKt + (2048 * t >> 4), dVp + (2048 * t >> 4), id_mnmn, t > 0);
                 mma_commit(&s.mma_s);
 #pragma unroll
                 for (int t = 0; t < 4; ++t)  // [A B ; 0] V_{c+1}
@@ -584,56 +643,57 @@ k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
         // --------------------------- math warps ----------------------------
         const int t = tid;  // TMEM lane and state row
         const int last_len = si.len - kChunk * (nc - 1);  // valid length of the last chunk
-        // Gamma_c Q_c in place (rows 64..127 of A1 of the step's buffer)
-        auto scale_q = [&](StepBuf &B) {
+        auto len_of = [&](int c) { return c == nc - 1 ? last_len : kChunk; };
+        // Readies a loaded step buffer for its MMAs, in place: rows r of Q_c
+        // scaled by gamma_r = exp(gc_r), rows i of K_c by d_{c,i} =
+        // exp(gc_{l-1} - gc_i) (zero for i >= l, which also clears rows that
+        // belong to the next sequence). Returns gamma_c = exp(gc_{l-1}).
+        // A step buffer goes back to the producer as soon as its MMAs
+        // complete, so nothing is read from it after that point.
+        auto ready_buffer = [&](StepBuf &B, int lc) {
+            const float glast = B.gbc[lc - 1];
 #pragma unroll
             for (int k2 = 0; k2 < 8; ++k2) {
                 const int p = t + kMathThreads * k2;  // 1024 chunks: 64 rows x 16
                 const int r = p >> 4, hf = (p >> 3) & 1, ch = p & 7;
-                uint8_t *ptr = B.A1 + hf * 2 * kTile + kTile + sw128_offset(r, ch);
-                float x[8];
-                unpack8(*reinterpret_cast<const uint4 *>(ptr), x);
+                uint8_t *qp = B.A1 + hf * 2 * kTile + kTile + sw128_offset(r, ch);
+                uint8_t *kp = B.Kt + hf * kTile + sw128_offset(r, ch);
+                float x[8], y[8];
+                unpack8(*reinterpret_cast<const uint4 *>(qp), x);
+                unpack8(*reinterpret_cast<const uint4 *>(kp), y);
                 const float gr = __expf(B.gbc[r]);
+                const float dr = r < lc ? __expf(glast - B.gbc[r]) : 0.f;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] *= gr;
-                *reinterpret_cast<uint4 *>(ptr) = pack8(x);
+                for (int e = 0; e < 8; ++e) {
+                    x[e] *= gr;
+                    y[e] *= dr;
+                }
+                *reinterpret_cast<uint4 *>(qp) = pack8(x);
+                *reinterpret_cast<uint4 *>(kp) = pack8(y);
             }
+            return __expf(glast);
         };
-        auto len_of = [&](int c) { return c == nc - 1 ? last_len : kChunk; };
-        // A step buffer is handed back to the producer as soon as the step's
-        // MMAs complete, so every value the epilogue needs from it (gamma_c,
-        // d_{c+1}) is read into registers while the buffer is known to hold
-        // this step's data: one step ahead, right after its copies land.
-        float gam_cur = 1.f, dn_cur = 0.f;  // gamma_c and d_{c+1}[t] of the current step
+        float gam_cur = 1.f;  // gamma_c of the current step (1 for the virtual step c = -1)
         if (nc > 0) {
-            if (!mbar_wait(&s.full[0], 0)) s.abort = 1;  // step -1 reads buffer 0 (no Q)
-            const int l0 = len_of(0);
-            dn_cur = t < l0 ? __expf(s.buf[0].gbn[l0 - 1] - s.buf[0].gbn[t]) : 0.f;
+            if (!mbar_wait(&s.full[0], 0)) s.abort = 1;  // step -1: nothing to scale
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&s.ready);
         }
         // an empty sequence has no steps at all (not even the virtual c = -1):
         // its final state is its initial state
         for (int c = -1; nc > 0 && c < nc && !s.abort; ++c) {
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&s.ready);
-            // next step's buffer: wait for its copies, scale its Q, take its gates
-            float gam_nxt = 1.f, dn_nxt = 0.f;
+            // (A) while step c's MMAs run: ready the next step's buffer
+            float gam_nxt = 1.f;
             if (c + 1 < nc) {
                 const int bn = (c + 2) & 1, usen = (c + 2) >> 1;
                 if (!mbar_wait(&s.full[bn], usen & 1)) {
                     s.abort = 1;
                     break;
                 }
-                StepBuf &N = s.buf[bn];
-                scale_q(N);
-                gam_nxt = __expf(N.gbc[len_of(c + 1) - 1]);
-                if (c + 2 < nc) {
-                    const int l2 = len_of(c + 2);
-                    dn_nxt = t < l2 ? __expf(N.gbn[l2 - 1] - N.gbn[t]) : 0.f;
-                }
+                gam_nxt = ready_buffer(s.buf[bn], len_of(c + 1));
             }
-            const int lc = c < 0 ? 0 : len_of(c);
-            // state update: S_{c+1}[t] = gamma_c S_c[t] + D2[t]
+            // (B) the chain: S_{c+1} and V'_{c+1} go to their operand buffers
             if (!mbar_wait(&s.mma_s, (c + 1) & 1)) {
                 s.abort = 1;
                 break;
@@ -647,7 +707,6 @@ k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
                 for (int e = 0; e < 64; ++e) Sr[e] = fmaf(gam_cur, Sr[e], v[e]);
             }
-            // D1 rows: V'_{c+1} (t < 64) or O_c (t >= 64)
             if (!mbar_wait(&s.mma, (c + 1) & 1)) {
                 s.abort = 1;
                 break;
@@ -657,24 +716,21 @@ k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
             for (int j = 0; j < 4; ++j) tmem_ld16(tmem_addr(tmem, 32 * warp, kTmD1 + 16 * j), d1 + 16 * j);
             tmem_ld_wait();
-            tc_fence_before();
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch)
                 *reinterpret_cast<uint4 *>(s.Sb + sw128_offset(t, ch)) = pack8(Sr + 8 * ch);
-            if (t < 64) {
-                if (c + 1 < nc) {
-                    float vd[8];
+            if (t < 64 && c + 1 < nc) {
 #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) vd[e] = dn_cur * d1[8 * ch + e];
-                        *reinterpret_cast<uint4 *>(s.Vp + sw128_offset(t, ch)) = pack8(d1 + 8 * ch);
-                        *reinterpret_cast<uint4 *>(s.Vd + sw128_offset(t, ch)) = pack8(vd);
-                    }
-                }
-            } else if (c >= 0) {
+                for (int ch = 0; ch < 8; ++ch)
+                    *reinterpret_cast<uint4 *>(s.Vp + sw128_offset(t, ch)) = pack8(d1 + 8 * ch);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            if (c + 1 < nc) mbar_arrive(&s.ready);
+            // (C) output rows of chunk c, overlapping step c+1's MMAs
+            if (t >= 64 && c >= 0) {
                 const int r = t - 64;
-                if (r < lc) {
+                if (r < len_of(c)) {
                     __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) +
                                           (size_t(si.start + kChunk * c + r) * a.hv + h) * kHeadDim + e0;
                     float o[8];
@@ -687,7 +743,6 @@ k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
                 }
             }
             gam_cur = gam_nxt;
-            dn_cur = dn_nxt;
         }
         if (!s.abort && a.final_state) {
             float4 *dst = reinterpret_cast<float4 *>(a.final_state + sbase + size_t(t) * kHeadDim + e0);
@@ -739,7 +794,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, void *ws_data, cudaStream_t 
         return e;
     if (a.max_chunks > 0 && T > 0) {
         LaunchScope scope(GDN_K_CHUNK_PREPARE_TC, s);
-        k_chunk_prepare_tc<<<dim3(a.max_chunks, a.hq), kPrepThreads, prep_smem, s>>>(a, w, tq, tk);
+        k_chunk_prepare_tc<<<dim3(a.max_chunks, a.hv), kPrepThreads, prep_smem, s>>>(a, w, tq, tk);
     }
     if ((e = cudaGetLastError())) return e;
     {
