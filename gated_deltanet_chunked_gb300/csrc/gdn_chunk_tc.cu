@@ -51,16 +51,16 @@ using namespace tc;
 constexpr uint32_t kTile = 64 * 128;  // bytes of a [64 rows][64 bf16] swizzled tile
 constexpr int kFPitch = 68;           // f32 row pitch of the solve matrices
 
-// per (chunk, v-head) outputs of the prepare kernel
-constexpr uint32_t kUnitAb = 0;               // A diag(beta)        [i][j]
-constexpr uint32_t kUnitW = kTile;            // -gamma_{c-1} W_c    [i][d], two d-halves
-constexpr uint32_t kUnitG = 3 * kTile;        // -G_{c-1}            [i][i']
-constexpr uint32_t kUnitP = 4 * kTile;        // P_c                 [r][i]
-constexpr uint32_t kUnitBytes = 5 * kTile;    // 40 KiB
+// per (chunk, v-head) outputs of the prepare kernel, bf16, 128B-swizzled rows
+constexpr uint32_t kUnitP = 0;              // P_c                  [r][j]  64 rows
+constexpr uint32_t kUnitW = kTile;          // -gamma_{c-1} W_c     [i][d]  64 rows, two d-halves
+constexpr uint32_t kUnitG = 3 * kTile;      // -K_{c-1} W_c^T       [t][i]  64 rows
+constexpr uint32_t kUnitU = 4 * kTile;      // U_c^T = (A B V)^T    [e][i] 128 rows
+constexpr uint32_t kUnitBytes = 6 * kTile;  // 48 KiB
 
 struct TcWs {
     uint8_t *unit;  // [max_chunks][hv][kUnitBytes]
-    float *gb;      // [max_chunks][hv][128]: gc[0..63], beta[0..63]
+    float *gb;      // [max_chunks][hv][128]: Gamma_r = exp(gc_r) (r < 64), then d_i (i < 64)
 };
 
 __host__ __device__ inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -119,24 +119,25 @@ __device__ __forceinline__ void warp_scan64(float &a0, float &a1, int lane) {
 constexpr int kPrepThreads = 128;
 
 struct PrepSmem {
-    alignas(1024) uint8_t KQ[4 * kTile];  // [K_c ; Q_c] K-major, M = 128 (two d-halves of 16 KiB)
+    // [K_c ; Q_c] K-major, M = 128 (two d-halves of 16 KiB: K rows, then Q
+    // rows). Once [K;Q]K^T is done the Q slots take V_c (for U^T), and once
+    // W_c is done the K slots take W_c bf16 (for K_{c-1} W_c^T).
+    alignas(1024) uint8_t KQ[4 * kTile];
     alignas(1024) uint8_t Kp[2 * kTile];  // K_{c-1}, two d-halves
     // A diag(beta gamma) bf16 [i][j]; before the solve ends it holds the raw
     // gates (g, gp) and the 16x16 block product T of the solve
     alignas(1024) uint8_t Ag[kTile];
-    alignas(1024) float MX[64 * kFPitch]; // M, inverted in place into A; later W_c bf16 [i][d]
+    alignas(1024) float MX[64 * kFPitch]; // M, inverted in place into A; then A diag(beta) bf16 [i][j]
     float beta[64], gc[64], gcp[64];
-    uint64_t bar_load, bar_mma;
+    uint64_t bar_load, bar_v, bar_mma;
     uint32_t tmem;
     int abort;
 };
 
-// MX (17 KiB) must also hold the bf16 W tile (16 KiB) once the solve is done
-static_assert(64 * kFPitch * sizeof(float) >= 2 * kTile, "W tile reuses the solve buffer");
 
 __global__ void __launch_bounds__(kPrepThreads, 3)
 k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm_q,
-                   const __grid_constant__ CUtensorMap tm_k) {
+                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
     extern __shared__ uint8_t smraw[];
     PrepSmem &s = *reinterpret_cast<PrepSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     const int c = blockIdx.x, h = blockIdx.y, hk = h / a.group;
@@ -161,6 +162,7 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
     if (tid == 0) {
         s.abort = 0;
         mbar_init(&s.bar_load, 1);
+        mbar_init(&s.bar_v, 1);
         mbar_init(&s.bar_mma, 1);
         fence_mbar_init();
         mbar_arrive_expect_tx(&s.bar_load, (has_prev ? 6u : 4u) * kTile);
@@ -216,35 +218,40 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
         dst[2 * lane + 1] = a1;
     }
     __syncthreads();
-    const float gp63 = s.gcp[63];  // read before gcp is overwritten with d_{c-1}
-    if (has_prev) gprev = -__expf(gp63);
-    __syncthreads();
+    if (has_prev) gprev = -__expf(s.gcp[63]);  // gamma_{c-1} = exp(sum of the gates of chunk c-1)
     // Decay factors exp(gc_r - gc_i), i <= r, from about 1.5K exponentials
     // instead of one per matrix entry. Within a 16-row block they are taken
     // directly; across blocks, with e(b) = 16 b + 15 the last row of block b,
     //   exp(gc_r - gc_i) = exp(gc_r - gc_e(b_i)) * exp(gc_e(b_i) - gc_i),
     // where both factors are <= 1 because the gates are log-decays (g <= 0,
-    // so gc does not increase along the chunk). gamma_j = exp(gc_j) and
-    // d_{c-1,i'} = exp(gc_{c-1,63} - gc_{c-1,i'}) are tabulated the same way.
+    // so gc does not increase along the chunk). The state walk gets
+    // Gamma_r = exp(gc_r) and d_i = exp(gc_{l-1} - gc_i) (zero for i >= l);
+    // the gates past l are zero, so gc_63 = gc_{l-1}.
     if (tid < 64) {
-        w.gb[unit * 128 + tid] = s.gc[tid];
-        w.gb[unit * 128 + 64 + tid] = s.beta[tid];
+        w.gb[unit * 128 + tid] = __expf(s.gc[tid]);
         colf[tid] = __expf(s.gc[16 * (tid >> 4) + 15] - s.gc[tid]);
 #pragma unroll
         for (int b = 0; b < 4; ++b) rowf[4 * tid + b] = b < (tid >> 4) ? __expf(s.gc[tid] - s.gc[16 * b + 15]) : 0.f;
     } else {
-        const int j = tid - 64;
-        s.gcp[j] = has_prev ? __expf(gp63 - s.gcp[j]) : 0.f;  // becomes d_{c-1}
+        const int i = tid - 64;
+        w.gb[unit * 128 + 64 + i] = i < l ? __expf(s.gc[63] - s.gc[i]) : 0.f;
     }
     for (int e = tid; e < 1024; e += kPrepThreads) {
         const int b = e >> 8, r = (e >> 4) & 15, i = e & 15;
         DB[(b * 16 + r) * kDBp + i] = i <= r ? __expf(s.gc[16 * b + r] - s.gc[16 * b + i]) : 0.f;
     }
-    if (!s.abort && !mbar_wait(&s.bar_mma, mma_phase)) s.abort = 1;
+    // warp-uniform outcome: the tcgen05 loads below are .sync.aligned
+    const bool ok_kq = __all_sync(0xffffffffu, !s.abort && mbar_wait(&s.bar_mma, mma_phase));
+    if (!ok_kq) s.abort = 1;
     mma_phase ^= 1;
     tc_fence_after();
+    // the Q slots are free: V_c goes there for U^T (needed only after the solve)
+    if (tid == 0 && !s.abort) {
+        mbar_arrive_expect_tx(&s.bar_v, 2 * kTile);
+        for (int hf = 0; hf < 2; ++hf) tma_load_3d(s.KQ + hf * 2 * kTile + kTile, &tm_v, 64 * hf, h, ci.start, &s.bar_v);
+    }
     // ---- M (rows 0-63: K K^T) and P (rows 64-127: Q K^T), one row per thread ----
-    if (!s.abort) {
+    if (ok_kq) {
         float v[64];
 #pragma unroll
         for (int j = 0; j < 4; ++j) tmem_ld16(tmem_addr(tmem, 32 * warp, 16 * j), v + 16 * j);
@@ -355,24 +362,35 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
             }
         }
     }
-    // ---- A diag(beta) -> global; A diag(beta gamma) -> smem operand ----
+    // ---- A diag(beta) and A diag(beta gamma) -> bf16 smem operands ----
     // (entries above the diagonal of A are exactly zero: the strictly upper
-    // part of M was never written with anything but zeros)
-    for (int p = tid; p < 512; p += kPrepThreads) {
-        const int i = p >> 3, ch = p & 7;
-        float x[8], y[8];
-        const float4 *xr = reinterpret_cast<const float4 *>(M + i * kFPitch + 8 * ch);
-        const float4 x0 = xr[0], x1 = xr[1];
-        x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
-        x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
+    // part of M was never written with anything but zeros). A diag(beta)
+    // overwrites the f32 solve buffer, so every thread reads its pieces first.
+    uint8_t *Ab = reinterpret_cast<uint8_t *>(s.MX);
+    {
+        float xs[4][8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int j = 8 * ch + e;
-            x[e] = (j <= i) ? x[e] * s.beta[j] : 0.f;
-            y[e] = x[e] * s.gc[j];  // gamma_j
+        for (int k2 = 0; k2 < 4; ++k2) {
+            const int p = tid + kPrepThreads * k2, i = p >> 3, ch = p & 7;
+            const float4 *xr = reinterpret_cast<const float4 *>(M + i * kFPitch + 8 * ch);
+            const float4 x0 = xr[0], x1 = xr[1];
+            xs[k2][0] = x0.x; xs[k2][1] = x0.y; xs[k2][2] = x0.z; xs[k2][3] = x0.w;
+            xs[k2][4] = x1.x; xs[k2][5] = x1.y; xs[k2][6] = x1.z; xs[k2][7] = x1.w;
         }
-        *reinterpret_cast<uint4 *>(uo + kUnitAb + sw128_offset(i, ch)) = pack8(x);
-        *reinterpret_cast<uint4 *>(s.Ag + sw128_offset(i, ch)) = pack8(y);
+        __syncthreads();
+#pragma unroll
+        for (int k2 = 0; k2 < 4; ++k2) {
+            const int p = tid + kPrepThreads * k2, i = p >> 3, ch = p & 7;
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int j = 8 * ch + e;
+                xs[k2][e] = (j <= i) ? xs[k2][e] * s.beta[j] : 0.f;
+                y[e] = xs[k2][e] * s.gc[j];  // gamma_j
+            }
+            *reinterpret_cast<uint4 *>(Ab + sw128_offset(i, ch)) = pack8(xs[k2]);
+            *reinterpret_cast<uint4 *>(s.Ag + sw128_offset(i, ch)) = pack8(y);
+        }
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -392,7 +410,6 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
     if (!s.abort && !mbar_wait(&s.bar_mma, mma_phase)) s.abort = 1;
     mma_phase ^= 1;
     tc_fence_after();
-    uint8_t *Wb = reinterpret_cast<uint8_t *>(s.MX);  // the solve buffer is free now
     {
         const int i = 16 * warp + lane;  // M=64 accumulator row (lanes 0-15)
 #pragma unroll
@@ -401,7 +418,7 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
             tmem_ld16(tmem_addr(tmem, 32 * warp, 16 * j), v);
             tmem_ld_wait();
             if (lane < 16) {
-                uint8_t *wbh = Wb + (j >> 2) * kTile;
+                uint8_t *wbh = s.KQ + (j >> 2) * 2 * kTile;  // K slot of d-half j/4 (K_c is done)
                 uint8_t *woh = uo + kUnitW + (j >> 2) * kTile;
                 float sv[16];
 #pragma unroll
@@ -416,42 +433,67 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    // ---- G_{c-1} = W_c K_{c-1}^T diag(d_{c-1}) : M=64, N=64, K=128 ----
-    if (has_prev) {
-        if (tid == 0 && !s.abort) {
+    // ---- U_c^T = V_c^T (A diag(beta))^T : M=128 (e), N=64 (i), K=64 (j),
+    //      V tile read as an MN-major A;  K_{c-1} W_c^T : M=64 (t), N=64 (i), K=128
+    if (tid == 0 && !s.abort) {
+        if (mbar_wait(&s.bar_v, 0)) {
             tc_fence_after();
-            const uint32_t wb = smem_u32(Wb), kp = smem_u32(s.Kp);
-            const uint32_t id = idesc_bf16_f32(64, 64, false, false);
+            const uint32_t kq = smem_u32(s.KQ), ab = smem_u32(Ab);
+            const uint32_t idu = idesc_bf16_f32(128, 64, true, false);
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const uint32_t off = (t >> 2) * kTile + (t & 3) * 32;
-                mma_bf16(tmem, sdesc_sw128(wb + off, 16, 1024), sdesc_sw128(kp + off, 16, 1024), id, t > 0);
+            for (int t = 0; t < 4; ++t)
+                mma_bf16(tmem, sdesc_sw128(kq + kTile + 2048 * t, 2 * kTile, 1024), sdesc_sw128(ab + 32 * t, 16, 1024),
+                         idu, t > 0);
+            if (has_prev) {
+                const uint32_t kp = smem_u32(s.Kp);
+                const uint32_t idg = idesc_bf16_f32(64, 64, false, false);
+#pragma unroll
+                for (int t = 0; t < 8; ++t)
+                    mma_bf16(tmem + 64, sdesc_sw128(kp + (t >> 2) * kTile + (t & 3) * 32, 16, 1024),
+                             sdesc_sw128(kq + (t >> 2) * 2 * kTile + (t & 3) * 32, 16, 1024), idg, t > 0);
             }
             mma_commit(&s.bar_mma);
+        } else {
+            s.abort = 1;
         }
-        __syncthreads();
-        if (!s.abort && !mbar_wait(&s.bar_mma, mma_phase)) s.abort = 1;
-        mma_phase ^= 1;
-        tc_fence_after();
-        const int i = 16 * warp + lane;
+    }
+    __syncthreads();
+    const bool ok_u = __all_sync(0xffffffffu, !s.abort && mbar_wait(&s.bar_mma, mma_phase));
+    if (!ok_u) s.abort = 1;
+    mma_phase ^= 1;
+    tc_fence_after();
+    if (ok_u) {
+        // U^T row e = tid (M=128: lane e)
         float v[64];
 #pragma unroll
         for (int j = 0; j < 4; ++j) tmem_ld16(tmem_addr(tmem, 32 * warp, 16 * j), v + 16 * j);
         tmem_ld_wait();
-        if (lane < 16) {
 #pragma unroll
-            for (int e = 0; e < 64; ++e) v[e] = -v[e] * s.gcp[e];  // d_{c-1}
+        for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<uint4 *>(uo + kUnitU + sw128_offset(tid, q)) = pack8(v + 8 * q);
+        if (has_prev) {
+            // row t = 16 warp + lane of -K_{c-1} W_c^T (M=64: lanes 0-15)
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                *reinterpret_cast<uint4 *>(uo + kUnitG + sw128_offset(i, q)) = pack8(v + 8 * q);
+            for (int j = 0; j < 4; ++j) tmem_ld16(tmem_addr(tmem + 64, 32 * warp, 16 * j), v + 16 * j);
+            tmem_ld_wait();
+            if (lane < 16) {
+                const int t = 16 * warp + lane;
+#pragma unroll
+                for (int e = 0; e < 64; ++e) v[e] = -v[e];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    *reinterpret_cast<uint4 *>(uo + kUnitG + sw128_offset(t, q)) = pack8(v + 8 * q);
+            }
         }
-    } else {
+    }
+    if (!has_prev) {
         for (int p = tid; p < int(kTile / 16); p += kPrepThreads)
             reinterpret_cast<uint4 *>(uo + kUnitG)[p] = make_uint4(0, 0, 0, 0);
     }
     if (s.abort && tid == 0) {
         record_status(a.status, GDN_ETIMEOUT);
         mbar_wait(&s.bar_load, 0, 100000000ull);  // bounded drain of the tile copies
+        mbar_wait(&s.bar_v, 0, 100000000ull);
     }
     tc_fence_before();
     __syncthreads();
@@ -459,26 +501,47 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
 }
 
 // ===========================================================================
-// k_chunk_state_output_tc
+// k_chunk_state_output_tc: one CTA per (sequence, v-head), 320 threads
 // ===========================================================================
-constexpr int kMathThreads = 128;
-constexpr int kStateThreads = 192;  // 4 math warps + producer warp + MMA warp
-constexpr int kDvTile = 64;
+// The walk runs transposed, with dv (e) as the MMA's M dimension so that the
+// whole 128-wide state of a head is one M=128 accumulator and the operands the
+// math warps produce each step (Sigma = S^T and X = V'^T) are written straight
+// into tensor memory as the A operands of the next step's MMAs:
+//   (c) [V'^T partial | Sigma_c Q_c^T] = Sigma_c [-gamma_c W_{c+1} ; Q_c]^T     N=128, K=128
+//   (a) [Sigma_{c+1} | V'^T partial] += X'_c [K_c | -K_c W_{c+1}^T]           N=192, K=64
+//       with X'_c = X_c diag(d_c) and the Sigma columns preloaded with gamma_c Sigma_c
+//   (b) X_c P_c^T                                                             N=64,  K=64
+// then V'^T_{c+1} = U^T_{c+1} + partial and O_c^T = scale (Sigma_c Q_c^T Gamma_c + X_c P_c^T).
+constexpr int kMathThreads = 256;   // 8 warps: lane quarter (warp % 4) x column half (warp / 4)
+constexpr int kStateThreads = 320;  // + copy warp (lane 0: MMA operands, lane 1: epilogue data) + MMA warp
+constexpr int kCopyWarp = 8, kMmaWarp = 9;
 
-struct StepBuf {
-    alignas(1024) uint8_t A0[2 * kTile];  // [A_{c+1} B ; 0]          K-major, M=128, K=64
-    alignas(1024) uint8_t A1[4 * kTile];  // [-W'_{c+1} ; Gamma_c Q_c] K-major, M=128, K=128 (two d-halves)
-    alignas(1024) uint8_t A2[2 * kTile];  // [-G_c ; P_c]             K-major, M=128, K=64
-    alignas(1024) uint8_t Bv[kTile];      // V_{c+1}[:, tile]         MN-major B, [j][e]
-    alignas(1024) uint8_t Kt[2 * kTile];  // diag(d_c) K_c             MN-major A (K^T), [i][d]
-    float gbc[128];                       // gc, beta of chunk c
+// tensor-memory columns (512 allocated)
+constexpr uint32_t kTmSig = 0;    // Sigma accumulator f32 [e][k], 128 columns
+constexpr uint32_t kTmV = 128;    // V'^T_{c+1} partial, 64 columns
+constexpr uint32_t kTmSQ = 192;   // Sigma_c Q_c^T, 64 columns
+constexpr uint32_t kTmXP = 256;   // X_c P_c^T, 64 columns
+constexpr uint32_t kTmSA = 320;   // Sigma_c bf16 A operand (K = 128), 64 columns
+constexpr uint32_t kTmXA = 384;   // X_c bf16 A operand (K = 64), two buffers of 32 columns
+constexpr uint32_t kTmXdA = 448;  // X'_c bf16 A operand, 32 columns
+
+struct BStage {                           // MMA operands of one step
+    alignas(1024) uint8_t B1[3 * kTile];  // [K_c (two d-halves) | -K_c W_{c+1}^T], MN-major rows t
+    alignas(1024) uint8_t Pc[kTile];      // P_c [r][j], K-major
+    alignas(1024) uint8_t B2[4 * kTile];  // per d-half: [-gamma_c W_{c+1} ; Q_c] rows, K-major
 };
-
+struct MStage {                           // what the math warps read in one step
+    alignas(1024) uint8_t Ut[2 * kTile];  // U^T_{c+1} [e][i]
+    float gbc[128];                       // Gamma_c, d_c
+    float gbn[128];                       // Gamma_{c+1}, d_{c+1}
+};
 struct StateSmem {
-    StepBuf buf[2];
-    alignas(1024) uint8_t Sb[2 * kTile];  // S_c bf16 [d][e] (128 rows), MN-major B
-    alignas(1024) uint8_t Vp[kTile];      // V'_c bf16 [i][e], MN-major B
-    uint64_t full[2], empty[2], ready, mma_s, mma;
+    BStage bs[2];
+    MStage ms[2];
+    // per math warp, two staging buffers of its 32 x 32 bf16 output block
+    // (rows r, 64-byte rows of e) for TMA stores
+    alignas(1024) uint8_t Ost[8][2][2048];
+    uint64_t fullB[2], emptyB[2], fullM[2], emptyM[2], ready_s, ready_x, mma, mma_o, o_free;
     uint32_t tmem;
     int abort;
 };
@@ -491,19 +554,23 @@ struct StateArgs {
 // dynamic shared memory per block is capped at 227 KiB; one more KiB is
 // requested to align the base to 1024 bytes
 static_assert(sizeof(StateSmem) + 1024 <= 227 * 1024, "state kernel shared memory");
-static_assert(sizeof(StepBuf) % 1024 == 0, "step buffers keep the 1024-byte swizzle alignment");
+static_assert(sizeof(BStage) % 1024 == 0 && sizeof(MStage) % 1024 == 0, "stages keep the swizzle alignment");
 // three CTAs per SM: 228 KiB per SM, 1 KiB reserved per CTA, 1 KiB alignment slack
 static_assert(3 * (sizeof(PrepSmem) + 2048) <= 228 * 1024, "three prepare CTAs per SM");
 
+__device__ __forceinline__ void pack_row(const float *x, uint32_t *r, int n2) {
+#pragma unroll
+    for (int j = 0; j < n2; ++j) r[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]);
+}
+
 __global__ void __launch_bounds__(kStateThreads, 1)
 k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
-                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
+                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_o) {
     extern __shared__ uint8_t smraw[];
     StateSmem &s = *reinterpret_cast<StateSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     const PrefillArgs &a = sa.a;
     const TcWs &w = sa.w;
-    const int tile = blockIdx.x & 1, n = blockIdx.x >> 1, h = blockIdx.y;
-    const int hk = h / a.group, e0 = tile * kDvTile;
+    const int n = blockIdx.x, h = blockIdx.y, hk = h / a.group;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (*a.n_chunks < 0) return;  // the chunk table rejected cu_seqlens
     const SeqInfo si = a.seq_info[n];
@@ -511,256 +578,325 @@ k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
     const size_t sbase = (size_t(n) * a.hv + h) * kHeadDim * kHeadDim;
 
     // zero every operand buffer once: regions a step does not load must hold
-    // finite values (their products land in rows that are discarded)
+    // finite values (their products land in columns that are discarded)
     for (uint32_t o = tid * 16; o < sizeof(StateSmem) - 64; o += kStateThreads * 16)
         *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(&s) + o) = make_uint4(0, 0, 0, 0);
     __syncthreads();
     if (tid == 0) {
         s.abort = 0;
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&s.full[b], 1);
-            mbar_init(&s.empty[b], 1);
+            mbar_init(&s.fullB[b], 1);
+            mbar_init(&s.emptyB[b], 1);
+            mbar_init(&s.fullM[b], 1);
+            mbar_init(&s.emptyM[b], kMathThreads);
         }
-        mbar_init(&s.ready, kMathThreads);
-        mbar_init(&s.mma_s, 1);
+        mbar_init(&s.ready_s, kMathThreads);
+        mbar_init(&s.ready_x, kMathThreads);
         mbar_init(&s.mma, 1);
+        mbar_init(&s.mma_o, 1);
+        mbar_init(&s.o_free, kMathThreads);
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(&s.tmem, 128);
+        tmem_alloc(&s.tmem, 512);
         tmem_relinquish();
     }
-    // initial state rows (thread t = row d = t) and its bf16 operand copy
-    float Sr[64];
-    if (tid < kMathThreads) {
-#pragma unroll
-        for (int q = 0; q < 64; ++q) Sr[q] = 0.f;
-        if (a.s0) {
-            const float4 *src = reinterpret_cast<const float4 *>(a.s0 + sbase + size_t(tid) * kHeadDim + e0);
-#pragma unroll
-            for (int q = 0; q < 16; ++q) {
-                const float4 v = src[q];
-                Sr[4 * q] = v.x; Sr[4 * q + 1] = v.y; Sr[4 * q + 2] = v.z; Sr[4 * q + 3] = v.w;
-            }
-        }
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-            *reinterpret_cast<uint4 *>(s.Sb + sw128_offset(tid, ch)) = pack8(Sr + 8 * ch);
-    }
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s.tmem;
-    const uint32_t kTmD1 = 0, kTmD2 = 64;
 
-    if (warp == 4) {
-        // ----------------------------- producer -----------------------------
+    if (warp == kCopyWarp) {
+        // --------------------------- copy thread ----------------------------
+        // one thread runs both rings, polling: the epilogue data of a step is
+        // released later than its MMA operands and must not hold back the
+        // next operand loads (two spinning lanes of one warp would starve
+        // each other)
         if (lane == 0 && nc > 0) {
             prefetch_tensormap(&tm_q);
             prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
-            for (int c = -1; c < nc && !s.abort; ++c) {
-                const int b = (c + 1) & 1, use = (c + 1) >> 1;
-                if (use > 0 && !mbar_wait(&s.empty[b], (use - 1) & 1)) {
-                    s.abort = 1;
-                    break;
-                }
-                StepBuf &B = s.buf[b];
-                uint32_t bytes = 0;
-                const bool cur = c >= 0, nxt = c + 1 < nc;
-                if (cur) bytes += 2 * kTile /*Q*/ + kTile /*P*/ + 2 * kTile /*K*/ + 512;
-                if (nxt) bytes += kTile /*Ab*/ + 2 * kTile /*W*/ + kTile /*G*/ + kTile /*V*/;
-                mbar_arrive_expect_tx(&s.full[b], bytes);
-                if (cur) {
-                    const int cg = si.first_chunk + c;
-                    const int start = si.start + kChunk * c;
-                    const uint8_t *uo = w.unit + (size_t(cg) * a.hv + h) * kUnitBytes;
-                    for (int hf = 0; hf < 2; ++hf) {
-                        tma_load_3d(B.A1 + hf * 2 * kTile + kTile, &tm_q, 64 * hf, hk, start, &s.full[b]);
-                        tma_load_3d(B.Kt + hf * kTile, &tm_k, 64 * hf, hk, start, &s.full[b]);
+            int cb = -1, cm = -1;  // next step whose operands / epilogue data are loaded
+            uint64_t t0 = globaltimer_ns();
+            while ((cb < nc || cm < nc) && !s.abort) {
+                bool progressed = false;
+                if (cb < nc) {
+                    const int c = cb, b = (c + 1) & 1, use = (c + 1) >> 1;
+                    if (use == 0 || mbar_try_wait(&s.emptyB[b], (use - 1) & 1)) {
+                        const bool cur = c >= 0, nxt = c + 1 < nc;
+                        BStage &B = s.bs[b];
+                        mbar_arrive_expect_tx(&s.fullB[b], (cur ? 5 * kTile : 0) + (nxt ? 3 * kTile : 0));
+                        if (cur) {
+                            const int start = si.start + kChunk * c;
+                            const uint8_t *uc = w.unit + (size_t(si.first_chunk + c) * a.hv + h) * kUnitBytes;
+                            for (int hf = 0; hf < 2; ++hf) {
+                                tma_load_3d(B.B1 + hf * kTile, &tm_k, 64 * hf, hk, start, &s.fullB[b]);
+                                tma_load_3d(B.B2 + hf * 2 * kTile + kTile, &tm_q, 64 * hf, hk, start, &s.fullB[b]);
+                            }
+                            bulk_load(B.Pc, uc + kUnitP, kTile, &s.fullB[b]);
+                        }
+                        if (nxt) {
+                            const uint8_t *un = w.unit + (size_t(si.first_chunk + c + 1) * a.hv + h) * kUnitBytes;
+                            for (int hf = 0; hf < 2; ++hf)
+                                bulk_load(B.B2 + hf * 2 * kTile, un + kUnitW + hf * kTile, kTile, &s.fullB[b]);
+                            bulk_load(B.B1 + 2 * kTile, un + kUnitG, kTile, &s.fullB[b]);
+                        }
+                        ++cb;
+                        progressed = true;
                     }
-                    bulk_load(B.A2 + kTile, uo + kUnitP, kTile, &s.full[b]);
-                    bulk_load(B.gbc, w.gb + (size_t(cg) * a.hv + h) * 128, 512, &s.full[b]);
                 }
-                if (nxt) {
-                    const int cg = si.first_chunk + c + 1;
-                    const int start = si.start + kChunk * (c + 1);
-                    const uint8_t *uo = w.unit + (size_t(cg) * a.hv + h) * kUnitBytes;
-                    bulk_load(B.A0, uo + kUnitAb, kTile, &s.full[b]);
-                    bulk_load(B.A1, uo + kUnitW, kTile, &s.full[b]);
-                    bulk_load(B.A1 + 2 * kTile, uo + kUnitW + kTile, kTile, &s.full[b]);
-                    bulk_load(B.A2, uo + kUnitG, kTile, &s.full[b]);
-                    tma_load_3d(B.Bv, &tm_v, e0, h, start, &s.full[b]);
+                if (cm < nc) {
+                    const int c = cm, b = (c + 1) & 1, use = (c + 1) >> 1;
+                    if (use == 0 || mbar_try_wait(&s.emptyM[b], (use - 1) & 1)) {
+                        const bool cur = c >= 0, nxt = c + 1 < nc;
+                        MStage &M = s.ms[b];
+                        mbar_arrive_expect_tx(&s.fullM[b], (cur ? 512 : 0) + (nxt ? 2 * kTile + 512 : 0));
+                        if (cur) bulk_load(M.gbc, w.gb + (size_t(si.first_chunk + c) * a.hv + h) * 128, 512, &s.fullM[b]);
+                        if (nxt) {
+                            const size_t un = size_t(si.first_chunk + c + 1) * a.hv + h;
+                            bulk_load(M.Ut, w.unit + un * kUnitBytes + kUnitU, 2 * kTile, &s.fullM[b]);
+                            bulk_load(M.gbn, w.gb + un * 128, 512, &s.fullM[b]);
+                        }
+                        ++cm;
+                        progressed = true;
+                    }
+                }
+                if (progressed) {
+                    t0 = globaltimer_ns();
+                } else if (globaltimer_ns() - t0 > 2000000000ull) {  // no slot freed for 2 s
+                    s.abort = 1;
+                }
+            }
+            if (s.abort) {  // bounded drain of copies that may be in flight
+                // last use of stage b among the steps -1 .. next-1 a ring has issued (-1: none)
+                auto last_use = [](int next, int b) {
+                    int c = next - 1;
+                    if (((c + 1) & 1) != b) --c;
+                    return c >= -1 ? (c + 1) >> 1 : -1;
+                };
+                for (int b = 0; b < 2; ++b) {
+                    const int ub = last_use(cb, b), um = last_use(cm, b);
+                    if (ub >= 0) mbar_wait(&s.fullB[b], ub & 1, 100000000ull);
+                    if (um >= 0) mbar_wait(&s.fullM[b], um & 1, 100000000ull);
                 }
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == kMmaWarp) {
         // ---------------------------- MMA issuer ----------------------------
         if (lane == 0 && nc > 0) {
-            const uint32_t id_kmn = idesc_bf16_f32(128, 64, false, true);
-            const uint32_t id_mnmn = idesc_bf16_f32(128, 64, true, true);
-            // descriptors of every operand base; a K step only adds its byte
-            // offset >> 4 to the start-address field (no carry: < 256 KiB)
-            const uint64_t dS = sdesc_sw128(smem_u32(s.Sb), kTile, 1024);
-            const uint64_t dVp = sdesc_sw128(smem_u32(s.Vp), kTile, 1024);
-            // the two step buffers differ by a constant byte offset
-            const uint64_t dA0_0 = sdesc_sw128(smem_u32(s.buf[0].A0), 16, 1024);
-            const uint64_t dA1_0 = sdesc_sw128(smem_u32(s.buf[0].A1), 16, 1024);
-            const uint64_t dA2_0 = sdesc_sw128(smem_u32(s.buf[0].A2), 16, 1024);
-            const uint64_t dBv_0 = sdesc_sw128(smem_u32(s.buf[0].Bv), kTile, 1024);
-            const uint64_t dKt_0 = sdesc_sw128(smem_u32(s.buf[0].Kt), kTile, 1024);
-            const uint64_t dbuf = uint64_t(sizeof(StepBuf) >> 4);
+            const uint32_t id_c = idesc_bf16_f32(128, 128, false, false);
+            const uint32_t id_a = idesc_bf16_f32(128, 192, false, true);
+            const uint32_t id_b = idesc_bf16_f32(128, 64, false, false);
+            // the two stages differ by a constant byte offset; a K step adds
+            // its byte offset >> 4 to the start-address field (no carry)
+            const uint64_t dB1 = sdesc_sw128(smem_u32(s.bs[0].B1), kTile, 1024);
+            const uint64_t dPc = sdesc_sw128(smem_u32(s.bs[0].Pc), 16, 1024);
+            const uint64_t dB2 = sdesc_sw128(smem_u32(s.bs[0].B2), 16, 1024);
+            const uint64_t dstage = uint64_t(sizeof(BStage) >> 4);
             for (int c = -1; c < nc && !s.abort; ++c) {
-                const int b = (c + 1) & 1;
-                if (!mbar_wait(&s.ready, (c + 1) & 1)) {
+                const int b = (c + 1) & 1, use = (c + 1) >> 1;
+                if (!mbar_wait(&s.ready_s, (c + 1) & 1) || !mbar_wait(&s.fullB[b], use & 1)) {
                     s.abort = 1;
                     break;
                 }
                 tc_fence_after();
-                const uint64_t ob = b ? dbuf : 0;
-                const uint64_t dA0 = dA0_0 + ob, dA1 = dA1_0 + ob, dA2 = dA2_0 + ob, dBv = dBv_0 + ob,
-                               dKt = dKt_0 + ob;
+                const uint64_t ob = b ? dstage : 0;
 #pragma unroll
-                for (int t = 0; t < 4; ++t)  // D2 = (diag(d_c) K_c)^T V'_c (state update first)
-                    mma_bf16(tmem + kTmD2, dKt + (2048 * t >> 4), dVp + (2048 * t >> 4), id_mnmn, t > 0);
-                mma_commit(&s.mma_s);
+                for (int t = 0; t < 8; ++t)  // (c) Sigma_c [-gamma_c W_{c+1} ; Q_c]^T
+                    mma_bf16_ts(tmem + kTmV, tmem + kTmSA + 8 * t,
+                                dB2 + ob + (((t >> 2) * 2 * kTile + (t & 3) * 32) >> 4), id_c, t > 0);
+                if (!mbar_wait(&s.ready_x, (c + 1) & 1)) {
+                    s.abort = 1;
+                    break;
+                }
+                tc_fence_after();
 #pragma unroll
-                for (int t = 0; t < 4; ++t)  // [A B ; 0] V_{c+1}
-                    mma_bf16(tmem + kTmD1, dA0 + (32 * t >> 4), dBv + (2048 * t >> 4), id_kmn, t > 0);
-#pragma unroll
-                for (int t = 0; t < 8; ++t)  // [-W' ; Gamma Q] S_c
-                    mma_bf16(tmem + kTmD1, dA1 + (((t >> 2) * 2 * kTile + (t & 3) * 32) >> 4),
-                             dS + (2048 * t >> 4), id_kmn, 1);
-#pragma unroll
-                for (int t = 0; t < 4; ++t)  // [-G ; P] V'_c
-                    mma_bf16(tmem + kTmD1, dA2 + (32 * t >> 4), dVp + (2048 * t >> 4), id_kmn, 1);
+                for (int t = 0; t < 4; ++t)  // (a) X'_c [K_c | -K_c W_{c+1}^T]
+                    mma_bf16_ts(tmem + kTmSig, tmem + kTmXdA + 8 * t, dB1 + ob + ((2048 * t) >> 4), id_a, 1);
                 mma_commit(&s.mma);
-                mma_commit(&s.empty[b]);
+                if (c >= 0) {
+                    if (c >= 1 && !mbar_wait(&s.o_free, (c - 1) & 1)) {
+                        s.abort = 1;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t xa = kTmXA + 32 * ((c + 1) & 1);
+#pragma unroll
+                    for (int t = 0; t < 4; ++t)  // (b) X_c P_c^T
+                        mma_bf16_ts(tmem + kTmXP, tmem + xa + 8 * t, dPc + ob + ((32 * t) >> 4), id_b, t > 0);
+                    mma_commit(&s.mma_o);
+                }
+                mma_commit(&s.emptyB[b]);
             }
         }
     } else {
         // --------------------------- math warps ----------------------------
-        const int t = tid;  // TMEM lane and state row
+        const int lq = warp & 3, ch = warp >> 2;  // TMEM lane quarter, column half
+        const int e = 32 * lq + lane;             // dv index = TMEM lane
+        const uint32_t lrow = uint32_t(32 * lq) << 16;
         const int last_len = si.len - kChunk * (nc - 1);  // valid length of the last chunk
-        auto len_of = [&](int c) { return c == nc - 1 ? last_len : kChunk; };
-        // Readies a loaded step buffer for its MMAs, in place: rows r of Q_c
-        // scaled by gamma_r = exp(gc_r), rows i of K_c by d_{c,i} =
-        // exp(gc_{l-1} - gc_i) (zero for i >= l, which also clears rows that
-        // belong to the next sequence). Returns gamma_c = exp(gc_{l-1}).
-        // A step buffer goes back to the producer as soon as its MMAs
-        // complete, so nothing is read from it after that point.
-        auto ready_buffer = [&](StepBuf &B, int lc) {
-            const float glast = B.gbc[lc - 1];
+        const size_t orow = size_t(a.hv) * kHeadDim;      // output row stride (elements)
+        // state columns k = 64 ch .. 64 ch + 63 of row e: Sigma_-1 = S0^T
+        {
+            float v[64];
 #pragma unroll
-            for (int k2 = 0; k2 < 8; ++k2) {
-                const int p = t + kMathThreads * k2;  // 1024 chunks: 64 rows x 16
-                const int r = p >> 4, hf = (p >> 3) & 1, ch = p & 7;
-                uint8_t *qp = B.A1 + hf * 2 * kTile + kTile + sw128_offset(r, ch);
-                uint8_t *kp = B.Kt + hf * kTile + sw128_offset(r, ch);
-                float x[8], y[8];
-                unpack8(*reinterpret_cast<const uint4 *>(qp), x);
-                unpack8(*reinterpret_cast<const uint4 *>(kp), y);
-                const float gr = __expf(B.gbc[r]);
-                const float dr = r < lc ? __expf(glast - B.gbc[r]) : 0.f;
+            for (int j = 0; j < 64; ++j) v[j] = a.s0 ? a.s0[sbase + size_t(64 * ch + j) * kHeadDim + e] : 0.f;
+            if (nc == 0) {  // empty sequence: no steps, the final state is S0
+                if (a.final_state) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    x[e] *= gr;
-                    y[e] *= dr;
+                    for (int j = 0; j < 64; ++j) a.final_state[sbase + size_t(64 * ch + j) * kHeadDim + e] = v[j];
                 }
-                *reinterpret_cast<uint4 *>(qp) = pack8(x);
-                *reinterpret_cast<uint4 *>(kp) = pack8(y);
+            } else {
+                uint32_t r[32];
+                tmem_st32(tmem + lrow + kTmSig + 64 * ch, reinterpret_cast<const uint32_t *>(v));
+                tmem_st32(tmem + lrow + kTmSig + 64 * ch + 32, reinterpret_cast<const uint32_t *>(v + 32));
+                pack_row(v, r, 32);
+                tmem_st32(tmem + lrow + kTmSA + 32 * ch, r);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) r[j] = 0u;
+                tmem_st16(tmem + lrow + kTmXA + 16 * ch, r);  // X_-1 = 0
+                tmem_st16(tmem + lrow + kTmXdA + 16 * ch, r);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&s.ready_s);
+                mbar_arrive(&s.ready_x);
             }
-            return __expf(glast);
-        };
-        float gam_cur = 1.f;  // gamma_c of the current step (1 for the virtual step c = -1)
-        if (nc > 0) {
-            if (!mbar_wait(&s.full[0], 0)) s.abort = 1;  // step -1: nothing to scale
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&s.ready);
         }
-        // an empty sequence has no steps at all (not even the virtual c = -1):
-        // its final state is its initial state
-        for (int c = -1; nc > 0 && c < nc && !s.abort; ++c) {
-            // (A) while step c's MMAs run: ready the next step's buffer
-            float gam_nxt = 1.f;
+        // every branch below is warp-uniform (the tcgen05 loads and stores
+        // are .sync.aligned): wait results and the abort flag are combined
+        // across the warp before they steer control flow
+        for (int c = -1; nc > 0 && c < nc && !__any_sync(0xffffffffu, s.abort); ++c) {
+            const int b = (c + 1) & 1, use = (c + 1) >> 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&s.mma, (c + 1) & 1) && mbar_wait(&s.fullM[b], use & 1))) {
+                s.abort = 1;
+                break;
+            }
+            tc_fence_after();
+            const MStage &M = s.ms[b];
+            float sq[32], x[32];
+            tmem_ld32(tmem + lrow + kTmSQ + 32 * ch, sq);
             if (c + 1 < nc) {
-                const int bn = (c + 2) & 1, usen = (c + 2) >> 1;
-                if (!mbar_wait(&s.full[bn], usen & 1)) {
+                // phase 1: Sigma_{c+1} as the bf16 A operand of the next (c), and
+                // gamma_{c+1} Sigma_{c+1} back into the accumulator for the next (a),
+                // read in two halves of 32 columns. Done while the tensor pipe is
+                // idle: TMEM stores slow down MMAs that run beside them. The next (c)
+                // overwrites the V'^T partial and Sigma Q^T columns, so both are read
+                // before it may start.
+                const float gam = M.gbn[63];  // gamma_{c+1}
+                tmem_ld32(tmem + lrow + kTmV + 32 * ch, x);
+#pragma unroll
+                for (int hq = 0; hq < 2; ++hq) {
+                    float v[32];
+                    tmem_ld32(tmem + lrow + kTmSig + 64 * ch + 32 * hq, v);
+                    tmem_ld_wait();
+                    uint32_t r[16];
+                    pack_row(v, r, 16);
+                    tmem_st16(tmem + lrow + kTmSA + 32 * ch + 16 * hq, r);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] *= gam;
+                    tmem_st32(tmem + lrow + kTmSig + 64 * ch + 32 * hq, reinterpret_cast<const uint32_t *>(v));
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&s.ready_s);
+                // phase 2 (overlaps the next (c)): X_{c+1} = U^T_{c+1} + partial and
+                // X' = X diag(d_{c+1})
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    float u[8];
+                    unpack8(*reinterpret_cast<const uint4 *>(M.Ut + sw128_offset(e, 4 * ch + q)), u);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) x[8 * q + j] += u[j];
+                }
+                uint32_t r[16];
+                pack_row(x, r, 16);
+                tmem_st16(tmem + lrow + kTmXA + 32 * (c & 1) + 16 * ch, r);  // X_{c+1}: buffer (c+2) & 1
+                const float4 *dn = reinterpret_cast<const float4 *>(M.gbn + 64 + 32 * ch);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 d4 = dn[q];
+                    x[4 * q] *= d4.x; x[4 * q + 1] *= d4.y; x[4 * q + 2] *= d4.z; x[4 * q + 3] *= d4.w;
+                }
+                pack_row(x, r, 16);
+                tmem_st16(tmem + lrow + kTmXdA + 16 * ch, r);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&s.ready_x);
+            } else {
+                float v[64];
+                tmem_ld32(tmem + lrow + kTmSig + 64 * ch, v);
+                tmem_ld32(tmem + lrow + kTmSig + 64 * ch + 32, v + 32);
+                tmem_ld_wait();
+                if (a.final_state) {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j)
+                        a.final_state[sbase + size_t(64 * ch + j) * kHeadDim + e] = v[j];
+                }
+            }
+            if (c >= 0) {
+                // O_c rows r = 32 ch + j, column e
+                if (!__all_sync(0xffffffffu, mbar_wait(&s.mma_o, c & 1))) {
                     s.abort = 1;
                     break;
                 }
-                gam_nxt = ready_buffer(s.buf[bn], len_of(c + 1));
-            }
-            // (B) the chain: S_{c+1} and V'_{c+1} go to their operand buffers
-            if (!mbar_wait(&s.mma_s, (c + 1) & 1)) {
-                s.abort = 1;
-                break;
-            }
-            tc_fence_after();
-            {
-                float v[64];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) tmem_ld16(tmem_addr(tmem, 32 * warp, kTmD2 + 16 * j), v + 16 * j);
+                tc_fence_after();
+                float o[32];
+                tmem_ld32(tmem + lrow + kTmXP + 32 * ch, o);
                 tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(&s.o_free);
+                const float4 *gm = reinterpret_cast<const float4 *>(M.gbc + 32 * ch);
 #pragma unroll
-                for (int e = 0; e < 64; ++e) Sr[e] = fmaf(gam_cur, Sr[e], v[e]);
-            }
-            if (!mbar_wait(&s.mma, (c + 1) & 1)) {
-                s.abort = 1;
-                break;
-            }
-            tc_fence_after();
-            float d1[64];
+                for (int q = 0; q < 8; ++q) {
+                    const float4 g4 = gm[q];
+                    o[4 * q] = a.scale * fmaf(g4.x, sq[4 * q], o[4 * q]);
+                    o[4 * q + 1] = a.scale * fmaf(g4.y, sq[4 * q + 1], o[4 * q + 1]);
+                    o[4 * q + 2] = a.scale * fmaf(g4.z, sq[4 * q + 2], o[4 * q + 2]);
+                    o[4 * q + 3] = a.scale * fmaf(g4.w, sq[4 * q + 3], o[4 * q + 3]);
+                }
+                // lanes e and e^1 swap so that each holds two adjacent columns of one row:
+                // even lanes rows 2m, odd lanes rows 2m + 1
+                const int odd = lane & 1;
+                uint32_t pr[16];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) tmem_ld16(tmem_addr(tmem, 32 * warp, kTmD1 + 16 * j), d1 + 16 * j);
-            tmem_ld_wait();
+                for (int m = 0; m < 16; ++m) {
+                    const float other = __shfl_xor_sync(0xffffffffu, odd ? o[2 * m] : o[2 * m + 1], 1);
+                    pr[m] = odd ? pack_bf16x2(other, o[2 * m + 1]) : pack_bf16x2(o[2 * m], other);
+                }
+                const int lc = c == nc - 1 ? last_len : kChunk;
+                const int row0 = si.start + kChunk * c + 32 * ch;  // token of the block's first row
+                // the TMA store writes all 32 rows unless they run past the tensor's
+                // end; rows past a sequence's end inside a packed batch take plain stores
+                if (32 * ch + 32 <= lc || si.start + si.len == a.total_tokens) {
+                    uint8_t *blk = s.Ost[warp][c & 1];
+                    if (lane == 0) bulk_wait_group_read<1>();  // the store from two steps ago has read blk
+                    __syncwarp();
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-                *reinterpret_cast<uint4 *>(s.Sb + sw128_offset(t, ch)) = pack8(Sr + 8 * ch);
-            if (t < 64 && c + 1 < nc) {
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch)
-                    *reinterpret_cast<uint4 *>(s.Vp + sw128_offset(t, ch)) = pack8(d1 + 8 * ch);
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            if (c + 1 < nc) mbar_arrive(&s.ready);
-            // (C) output rows of chunk c, overlapping step c+1's MMAs
-            if (t >= 64 && c >= 0) {
-                const int r = t - 64;
-                if (r < len_of(c)) {
-                    __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(a.out) +
-                                          (size_t(si.start + kChunk * c + r) * a.hv + h) * kHeadDim + e0;
-                    float o[8];
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) o[e] = a.scale * d1[8 * ch + e];
-                        reinterpret_cast<uint4 *>(orow)[ch] = pack8(o);
+                    for (int m = 0; m < 16; ++m)
+                        *reinterpret_cast<uint32_t *>(blk + (2 * m + odd) * 64 + 4 * (lane >> 1)) = pr[m];
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&tm_o, 32 * lq, h, row0, blk);
+                        bulk_commit_group();
                     }
+                } else {
+                    __nv_bfloat16 *obase =
+                        static_cast<__nv_bfloat16 *>(a.out) + (size_t(row0 + odd) * a.hv + h) * kHeadDim + (e & ~1);
+#pragma unroll
+                    for (int m = 0; m < 16; ++m)
+                        if (32 * ch + 2 * m + odd < lc)
+                            *reinterpret_cast<uint32_t *>(obase + size_t(2 * m) * orow) = pr[m];
                 }
             }
-            gam_cur = gam_nxt;
+            mbar_arrive(&s.emptyM[b]);
         }
-        if (!s.abort && a.final_state) {
-            float4 *dst = reinterpret_cast<float4 *>(a.final_state + sbase + size_t(t) * kHeadDim + e0);
-#pragma unroll
-            for (int q = 0; q < 16; ++q) dst[q] = make_float4(Sr[4 * q], Sr[4 * q + 1], Sr[4 * q + 2], Sr[4 * q + 3]);
-        }
+        if (lane == 0) bulk_wait_group_all();  // output stores complete before the CTA exits
     }
     __syncthreads();
-    if (s.abort) {
-        if (tid == 0) record_status(a.status, GDN_ETIMEOUT);
-        if (tid == kMathThreads) {  // bounded drain of copies that may be in flight
-            mbar_wait(&s.full[0], 0, 100000000ull);
-            mbar_wait(&s.full[1], 0, 100000000ull);
-        }
-    }
+    if (s.abort && tid == 0) record_status(a.status, GDN_ETIMEOUT);
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 128);
+    if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 }  // namespace
@@ -772,17 +908,20 @@ size_t prefill_tc_workspace(int max_chunks, int hv) {
 
 cudaError_t launch_prefill_tc(const PrefillArgs &a, void *ws_data, cudaStream_t s) {
     const TcWs w = tc_carve(ws_data, a.max_chunks, a.hv);
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     const uint64_t T = uint64_t(a.total_tokens);
     memset(&tq, 0, sizeof(tq));
     memset(&tk, 0, sizeof(tk));
     memset(&tv, 0, sizeof(tv));
+    memset(&to, 0, sizeof(to));
     // with no tokens every sequence is empty: the state kernel only copies
     // S0 to the final state and never touches the (then unset) tensor maps
     if (T > 0 &&
         (!make_tmap_bf16_3d(&tq, a.q, kHeadDim, a.hq, T, kHeadDim * 2, uint64_t(a.hq) * kHeadDim * 2, 64, 1, 64) ||
          !make_tmap_bf16_3d(&tk, a.k, kHeadDim, a.hq, T, kHeadDim * 2, uint64_t(a.hq) * kHeadDim * 2, 64, 1, 64) ||
-         !make_tmap_bf16_3d(&tv, a.v, kHeadDim, a.hv, T, kHeadDim * 2, uint64_t(a.hv) * kHeadDim * 2, 64, 1, 64)))
+         !make_tmap_bf16_3d(&tv, a.v, kHeadDim, a.hv, T, kHeadDim * 2, uint64_t(a.hv) * kHeadDim * 2, 64, 1, 64) ||
+         !make_tmap_bf16_3d(&to, a.out, kHeadDim, a.hv, T, kHeadDim * 2, uint64_t(a.hv) * kHeadDim * 2, 32, 1, 32,
+                            false)))
         return cudaErrorInvalidValue;
     const size_t prep_smem = sizeof(PrepSmem) + 1024;
     const size_t state_smem = sizeof(StateSmem) + 1024;
@@ -794,13 +933,13 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, void *ws_data, cudaStream_t 
         return e;
     if (a.max_chunks > 0 && T > 0) {
         LaunchScope scope(GDN_K_CHUNK_PREPARE_TC, s);
-        k_chunk_prepare_tc<<<dim3(a.max_chunks, a.hv), kPrepThreads, prep_smem, s>>>(a, w, tq, tk);
+        k_chunk_prepare_tc<<<dim3(a.max_chunks, a.hv), kPrepThreads, prep_smem, s>>>(a, w, tq, tk, tv);
     }
     if ((e = cudaGetLastError())) return e;
     {
         LaunchScope scope(GDN_K_STATE_OUTPUT_TC, s);
         StateArgs sa{a, w};
-        k_chunk_state_output_tc<<<dim3(2 * a.num_seqs, a.hv), kStateThreads, state_smem, s>>>(sa, tq, tk, tv);
+        k_chunk_state_output_tc<<<dim3(a.num_seqs, a.hv), kStateThreads, state_smem, s>>>(sa, tq, tk, to);
     }
     return cudaGetLastError();
 }

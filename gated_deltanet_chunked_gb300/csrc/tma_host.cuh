@@ -27,8 +27,12 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // 3-D bf16 tensor [d2][d1][d0] (d0 contiguous) with byte strides s1 (between
 // d1 rows) and s2 (between d2 slabs), copied in boxes of b0 x b1 x b2 with the
 // 128-byte swizzle; out-of-range elements read as zero.
+// With swizzle = false the box lands in shared memory as plain row-major
+// rows of b0 elements (used for stores: elements outside the tensor are not
+// written).
 inline bool make_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
-                              uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
+                              uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2,
+                              bool swizzle = true) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     const cuuint64_t dims[3] = {d0, d1, d2};
@@ -36,8 +40,8 @@ inline bool make_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t d0, u
     const cuuint32_t box[3] = {b0, b1, b2};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace gdn

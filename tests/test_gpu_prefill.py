@@ -54,6 +54,20 @@ def test_ragged_cases(cuda, dtype, lengths, hq, hv, with_s0):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("g_mu", [-6.0, -2.0, 4.0], ids=["weak", "medium", "underflow"])
+def test_decay_regimes(cuda, dtype, g_mu):
+    # g = -softplus(N(g_mu, 1)): weak decay keeps the per-chunk decay gamma near
+    # 0.8 (the running product of the gammas stays far from underflow over 16
+    # chunks), medium decay takes it to ~2^-19, and g_mu = 4 makes
+    # gamma = exp(~-256) underflow to zero in f32
+    inp = W.make_custom_prefill(31 + int(g_mu), [1000, 77], 1, 2, dtype, s0_sigma=0.1, g_mu=g_mu)
+    o, S = run_gpu_prefill(inp, cuda)
+    o_ref, S_ref = oracle_prefill(inp)
+    check(o, o_ref, dtype, "o")
+    check(S, S_ref, dtype, "final_state")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
 def test_dense_layout_equals_packed(cuda, dtype):
     inp = W.make_custom_prefill(7, [100, 100], 2, 4, dtype, s0_sigma=0.05)
     o_p, S_p = run_gpu_prefill(inp, cuda)
