@@ -95,6 +95,18 @@ __device__ __forceinline__ void unpack8(const uint4 u, float *x) {
     }
 }
 
+// e^x for the decay exponents (x <= 0: sums of log-decay gates), written as
+// 2^(x log2 e) on the special-function unit's base-2 exponential (PTX
+// ex2.approx.ftz.f32, relative error near 2^-22 per the PTX ISA). Results
+// below the smallest normal float flush to zero, which is the limit of a
+// decay factor; the product x log2 e adds a relative error of about
+// |x| 2^-24, negligible against the bf16 operands these factors scale.
+__device__ __forceinline__ float exp_decay(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x * 1.4426950408889634f));
+    return y;
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
@@ -153,11 +165,7 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
     // scratch in the Ag region, all consumed before Ag is written
     float *graw = reinterpret_cast<float *>(s.Ag);  // [64] gates of chunk c
     float *gpraw = graw + 64;                       // [64] gates of chunk c-1
-    float *T = graw + 128;                          // [256] block product of the solve
-    float *colf = graw + 384;                       // [64]  exp(gc_{e(j)} - gc_j)
-    float *rowf = graw + 448;                       // [64][4] exp(gc_i - gc_{e(b)}), b < i/16
-    float *DB = graw + 704;                         // [4][16][17] exp(gc_r - gc_i) within a block
-    constexpr int kDBp = 17;                        // padded row: lanes of a warp hit distinct banks
+    float *T = graw + 128;                          // [3][256] block products of the solve
 
     if (tid == 0) {
         s.abort = 0;
@@ -218,27 +226,14 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
         dst[2 * lane + 1] = a1;
     }
     __syncthreads();
-    if (has_prev) gprev = -__expf(s.gcp[63]);  // gamma_{c-1} = exp(sum of the gates of chunk c-1)
-    // Decay factors exp(gc_r - gc_i), i <= r, from about 1.5K exponentials
-    // instead of one per matrix entry. Within a 16-row block they are taken
-    // directly; across blocks, with e(b) = 16 b + 15 the last row of block b,
-    //   exp(gc_r - gc_i) = exp(gc_r - gc_e(b_i)) * exp(gc_e(b_i) - gc_i),
-    // where both factors are <= 1 because the gates are log-decays (g <= 0,
-    // so gc does not increase along the chunk). The state walk gets
-    // Gamma_r = exp(gc_r) and d_i = exp(gc_{l-1} - gc_i) (zero for i >= l);
-    // the gates past l are zero, so gc_63 = gc_{l-1}.
+    if (has_prev) gprev = -exp_decay(s.gcp[63]);  // gamma_{c-1} = exp(sum of the gates of chunk c-1)
+    // The state walk gets Gamma_r = exp(gc_r) and d_i = exp(gc_{l-1} - gc_i)
+    // (zero for i >= l); the gates past l are zero, so gc_63 = gc_{l-1}.
     if (tid < 64) {
-        w.gb[unit * 128 + tid] = __expf(s.gc[tid]);
-        colf[tid] = __expf(s.gc[16 * (tid >> 4) + 15] - s.gc[tid]);
-#pragma unroll
-        for (int b = 0; b < 4; ++b) rowf[4 * tid + b] = b < (tid >> 4) ? __expf(s.gc[tid] - s.gc[16 * b + 15]) : 0.f;
+        w.gb[unit * 128 + tid] = exp_decay(s.gc[tid]);
     } else {
         const int i = tid - 64;
-        w.gb[unit * 128 + 64 + i] = i < l ? __expf(s.gc[63] - s.gc[i]) : 0.f;
-    }
-    for (int e = tid; e < 1024; e += kPrepThreads) {
-        const int b = e >> 8, r = (e >> 4) & 15, i = e & 15;
-        DB[(b * 16 + r) * kDBp + i] = i <= r ? __expf(s.gc[16 * b + r] - s.gc[16 * b + i]) : 0.f;
+        w.gb[unit * 128 + 64 + i] = i < l ? exp_decay(s.gc[63] - s.gc[i]) : 0.f;
     }
     // warp-uniform outcome: the tcgen05 loads below are .sync.aligned
     const bool ok_kq = __all_sync(0xffffffffu, !s.abort && mbar_wait(&s.bar_mma, mma_phase));
@@ -256,26 +251,37 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
 #pragma unroll
         for (int j = 0; j < 4; ++j) tmem_ld16(tmem_addr(tmem, 32 * warp, 16 * j), v + 16 * j);
         tmem_ld_wait();
-        const int r = tid & 63, br = r >> 4;  // row (of M or P) and its 16-block
-        const float *db = DB + (br * 16 + (r & 15)) * kDBp;
-        float rf[4];
+        // Decay factor of column i in row r: exp(gc_r - gc_i) for i <= r. The
+        // gates are log-decays (g <= 0), so gc does not increase along the
+        // chunk and the exponent is never positive: no overflow, and a decay
+        // too strong for f32 flushes to zero. Columns past the warp's last row
+        // are zero for the whole warp and skipped.
+        const int r = tid & 63;            // row of M (warps 0-1) or P (warps 2-3)
+        const int rmax = (tid & 32) + 31;  // last row held by this warp
+        const float gr = s.gc[r];
+        const bool live = r < l;
+        const float sr = warp < 2 ? s.beta[r] : 1.f;  // M rows carry beta_r
+        const int strict = warp < 2 ? 1 : 0;          // M is strictly lower, P includes the diagonal
 #pragma unroll
-        for (int b = 0; b < 4; ++b) rf[b] = rowf[4 * r + b];
-        // decay factor of column i for row r (i <= r), 0 otherwise
-        auto decay = [&](int i) {
-            const int bi = i >> 4;
-            return bi == br ? db[i & 15] : (bi < br ? rf[bi] * colf[i] : 0.f);
-        };
+        for (int q = 0; q < 16; ++q) {
+            const float4 g4 = reinterpret_cast<const float4 *>(s.gc)[q];  // same address in every lane
+            const float gq[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+            for (int k2 = 0; k2 < 4; ++k2) {
+                const int i = 4 * q + k2;
+                if (i <= rmax) {
+                    const bool on = live && i + strict <= r;
+                    v[i] = on ? sr * exp_decay(gr - gq[k2]) * v[i] : 0.f;
+                } else {
+                    v[i] = 0.f;
+                }
+            }
+        }
         if (warp < 2) {
-            const float bi = s.beta[r];
-#pragma unroll
-            for (int j = 0; j < 64; ++j) v[j] = (j < r && r < l) ? bi * decay(j) * v[j] : 0.f;
             float4 *row = reinterpret_cast<float4 *>(M + r * kFPitch);
 #pragma unroll
             for (int q = 0; q < 16; ++q) row[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         } else {
-#pragma unroll
-            for (int i = 0; i < 64; ++i) v[i] = (i <= r && r < l) ? decay(i) * v[i] : 0.f;
 #pragma unroll
             for (int q = 0; q < 8; ++q)
                 *reinterpret_cast<uint4 *>(uo + kUnitP + sw128_offset(r, q)) = pack8(v + 8 * q);
@@ -283,8 +289,8 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
     }
     tc_fence_before();
     __syncthreads();
-    if (tid < 64) s.gc[tid] = __expf(s.gc[tid]);  // gc -> gamma (read only by the A diag(beta gamma) step)
-    // ---- A = (I + M)^-1 in place, 16x16 blocks ----
+    if (tid < 64) s.gc[tid] = exp_decay(s.gc[tid]);  // gc -> gamma (read only by the A diag(beta gamma) step)
+    // ---- A = (I + M)^-1, 16x16 blocks ----
 
     // diagonal blocks: thread = (block, column); column kept in registers
     if (tid < 64) {
@@ -313,20 +319,28 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
         for (int ii = 0; ii < 16; ++ii) M[(16 * b + ii) * kFPitch + 16 * b + jj] = x[ii];
     }
     __syncthreads();
-    // off-diagonal blocks, column block j left to right, rows i = j+1..3:
-
-    //   X_ij = -X_ii sum_{k=j}^{i-1} L_ik X_kj; L_ij is overwritten by X_ij,
-    //   which is safe because later blocks only read L_ik with k > j
+    // off-diagonal blocks by anti-diagonal levels, the blocks of a level in
+    // parallel:  level 1: (1,0) (2,1) (3,2);  level 2: (2,0) (3,1);  level 3: (3,0)
+    //   T_ij = sum_{k=j}^{i-1} L_ik X_kj,   X_ij = -X_ii T_ij
+    // X_ij (i > j) goes to the mirror block (j, i) of the strict upper
+    // triangle (zero until now), because later levels still read the
+    // original L blocks below the diagonal.
     {
-        const int ii = tid >> 3, jj = 2 * (tid & 7);  // two adjacent outputs per thread
-#pragma unroll 1
-        for (int j = 0; j < 3; ++j) {
-#pragma unroll 1
-            for (int i = j + 1; i < 4; ++i) {
+        const int ii = tid >> 3, jj = 2 * (tid & 7);  // two adjacent outputs per thread and block
+        auto xblk = [&](int k, int j) -> const float * {  // X_kj, k >= j
+            return k == j ? M + (16 * k) * kFPitch + 16 * k : M + (16 * j) * kFPitch + 16 * k;
+        };
+#pragma unroll
+        for (int lev = 1; lev <= 3; ++lev) {
+            const int nb = 4 - lev;  // blocks (j + lev, j), j = 0 .. nb-1
+#pragma unroll
+            for (int j = 0; j < nb; ++j) {
+                const int i = j + lev;
                 float t0 = 0.f, t1 = 0.f;
+#pragma unroll
                 for (int k = j; k < i; ++k) {
                     const float4 *Lr = reinterpret_cast<const float4 *>(M + (16 * i + ii) * kFPitch + 16 * k);
-                    const float *Xc = M + (16 * k) * kFPitch + 16 * j + jj;
+                    const float *Xc = xblk(k, j) + jj;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const float4 lq = Lr[q];
@@ -340,39 +354,45 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
                         t0 = fmaf(lq.w, x3.x, t0); t1 = fmaf(lq.w, x3.y, t1);
                     }
                 }
-                T[ii * 16 + jj] = t0;
-                T[ii * 16 + jj + 1] = t1;
-                __syncthreads();
+                *reinterpret_cast<float2 *>(&T[j * 256 + ii * 16 + jj]) = make_float2(t0, t1);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int j = 0; j < nb; ++j) {
+                const int i = j + lev;
                 const float4 *Xr = reinterpret_cast<const float4 *>(M + (16 * i + ii) * kFPitch + 16 * i);
                 float o0 = 0.f, o1 = 0.f;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const float4 xq = Xr[q];  // X_ii row (zero above the diagonal)
-                    const float2 u0 = *reinterpret_cast<const float2 *>(&T[(4 * q + 0) * 16 + jj]);
-                    const float2 u1 = *reinterpret_cast<const float2 *>(&T[(4 * q + 1) * 16 + jj]);
-                    const float2 u2 = *reinterpret_cast<const float2 *>(&T[(4 * q + 2) * 16 + jj]);
-                    const float2 u3 = *reinterpret_cast<const float2 *>(&T[(4 * q + 3) * 16 + jj]);
+                    const float2 u0 = *reinterpret_cast<const float2 *>(&T[j * 256 + (4 * q + 0) * 16 + jj]);
+                    const float2 u1 = *reinterpret_cast<const float2 *>(&T[j * 256 + (4 * q + 1) * 16 + jj]);
+                    const float2 u2 = *reinterpret_cast<const float2 *>(&T[j * 256 + (4 * q + 2) * 16 + jj]);
+                    const float2 u3 = *reinterpret_cast<const float2 *>(&T[j * 256 + (4 * q + 3) * 16 + jj]);
                     o0 = fmaf(xq.x, u0.x, o0); o1 = fmaf(xq.x, u0.y, o1);
                     o0 = fmaf(xq.y, u1.x, o0); o1 = fmaf(xq.y, u1.y, o1);
                     o0 = fmaf(xq.z, u2.x, o0); o1 = fmaf(xq.z, u2.y, o1);
                     o0 = fmaf(xq.w, u3.x, o0); o1 = fmaf(xq.w, u3.y, o1);
                 }
-                *reinterpret_cast<float2 *>(M + (16 * i + ii) * kFPitch + 16 * j + jj) = make_float2(-o0, -o1);
-                __syncthreads();
+                *reinterpret_cast<float2 *>(M + (16 * j + ii) * kFPitch + 16 * i + jj) = make_float2(-o0, -o1);
             }
+            __syncthreads();
         }
     }
     // ---- A diag(beta) and A diag(beta gamma) -> bf16 smem operands ----
-    // (entries above the diagonal of A are exactly zero: the strictly upper
-    // part of M was never written with anything but zeros). A diag(beta)
-    // overwrites the f32 solve buffer, so every thread reads its pieces first.
+    // (A is unit lower triangular: the mask j <= i zeroes everything above
+    // the diagonal, where the mirror blocks now sit). A diag(beta) overwrites
+    // the f32 solve buffer, so every thread reads its pieces first.
     uint8_t *Ab = reinterpret_cast<uint8_t *>(s.MX);
     {
         float xs[4][8];
 #pragma unroll
         for (int k2 = 0; k2 < 4; ++k2) {
             const int p = tid + kPrepThreads * k2, i = p >> 3, ch = p & 7;
-            const float4 *xr = reinterpret_cast<const float4 *>(M + i * kFPitch + 8 * ch);
+            // block (i/16, ch/2) of A; below the diagonal it sits in the mirror block
+            const int bi = i >> 4, bj = ch >> 1;
+            const float4 *xr = reinterpret_cast<const float4 *>(
+                bj < bi ? M + (16 * bj + (i & 15)) * kFPitch + 16 * bi + 8 * (ch & 1) : M + i * kFPitch + 8 * ch);
             const float4 x0 = xr[0], x1 = xr[1];
             xs[k2][0] = x0.x; xs[k2][1] = x0.y; xs[k2][2] = x0.z; xs[k2][3] = x0.w;
             xs[k2][4] = x1.x; xs[k2][5] = x1.y; xs[k2][6] = x1.z; xs[k2][7] = x1.w;
@@ -410,6 +430,8 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
     if (!s.abort && !mbar_wait(&s.bar_mma, mma_phase)) s.abort = 1;
     mma_phase ^= 1;
     tc_fence_after();
+    // free now: Ag (the W operand) and the solve buffer past A diag(beta)
+    uint8_t *wst1 = reinterpret_cast<uint8_t *>(s.MX) + kTile;
     {
         const int i = 16 * warp + lane;  // M=64 accumulator row (lanes 0-15)
 #pragma unroll
@@ -419,7 +441,7 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
             tmem_ld_wait();
             if (lane < 16) {
                 uint8_t *wbh = s.KQ + (j >> 2) * 2 * kTile;  // K slot of d-half j/4 (K_c is done)
-                uint8_t *woh = uo + kUnitW + (j >> 2) * kTile;
+                uint8_t *woh = (j >> 2) ? wst1 : s.Ag;        // staging of -gamma_{c-1} W_c for a bulk store
                 float sv[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) sv[e] = gprev * v[e];
@@ -433,6 +455,11 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
+    if (tid == 0) {  // whole 8 KiB tiles: one bulk copy each instead of scattered 16-byte stores
+        bulk_store(uo + kUnitW, s.Ag, kTile);
+        bulk_store(uo + kUnitW + kTile, wst1, kTile);
+        bulk_commit_group();
+    }
     // ---- U_c^T = V_c^T (A diag(beta))^T : M=128 (e), N=64 (i), K=64 (j),
     //      V tile read as an MN-major A;  K_{c-1} W_c^T : M=64 (t), N=64 (i), K=128
     if (tid == 0 && !s.abort) {
@@ -468,9 +495,12 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
 #pragma unroll
         for (int j = 0; j < 4; ++j) tmem_ld16(tmem_addr(tmem, 32 * warp, 16 * j), v + 16 * j);
         tmem_ld_wait();
+        // staged in the V slots (V is done): rows 0-63 and 64-127 are the two
+        // 8 KiB halves of the tile, with the same swizzle (it depends on row % 8)
+        uint8_t *ust = s.KQ + (tid >> 6) * 2 * kTile + kTile;
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<uint4 *>(uo + kUnitU + sw128_offset(tid, q)) = pack8(v + 8 * q);
+            *reinterpret_cast<uint4 *>(ust + sw128_offset(tid & 63, q)) = pack8(v + 8 * q);
         if (has_prev) {
             // row t = 16 warp + lane of -K_{c-1} W_c^T (M=64: lanes 0-15)
 #pragma unroll
@@ -481,14 +511,25 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
 #pragma unroll
                 for (int e = 0; e < 64; ++e) v[e] = -v[e];
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    *reinterpret_cast<uint4 *>(uo + kUnitG + sw128_offset(t, q)) = pack8(v + 8 * q);
+                for (int q = 0; q < 8; ++q)  // staged in the first W slot (the last MMA is done)
+                    *reinterpret_cast<uint4 *>(s.KQ + sw128_offset(t, q)) = pack8(v + 8 * q);
             }
         }
     }
     if (!has_prev) {
         for (int p = tid; p < int(kTile / 16); p += kPrepThreads)
             reinterpret_cast<uint4 *>(uo + kUnitG)[p] = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+        if (ok_u) {
+            bulk_store(uo + kUnitU, s.KQ + kTile, kTile);
+            bulk_store(uo + kUnitU + kTile, s.KQ + 3 * kTile, kTile);
+            if (has_prev) bulk_store(uo + kUnitG, s.KQ, kTile);
+            bulk_commit_group();
+        }
+        bulk_wait_group_all();  // every bulk store has completed before the CTA exits
     }
     if (s.abort && tid == 0) {
         record_status(a.status, GDN_ETIMEOUT);

@@ -86,6 +86,14 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, int x, int 
                  : "memory");
 }
 
+// Linear bulk copy shared -> global (16-byte aligned, size a multiple of 16),
+// tracked by bulk groups like the tensor stores.
+__device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 ::"l"(reinterpret_cast<uint64_t>(dst)), "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // waits until at most N committed store groups still read their shared source
