@@ -74,8 +74,7 @@ def kernel_bytes(name, T, N, hq, hv, io_bytes=2, s0=False, final=True, d=128):
         "prep_simt": qk + vv + gb,
         "state_simt": qk + st,
         "output_simt": 2 * qk + vv,
-        "chunk_prepare_tc": qk + gb,
-        "chunk_state_output_tc": 2 * qk + 2 * vv + gb + st,
+        "chunk_fused_tc": 2 * qk + 2 * vv + gb + st,
     }.get(name)
 
 

@@ -87,7 +87,7 @@ using namespace gdn;
 
 extern "C" {
 
-int gdn_version(void) { return 100; }
+int gdn_version(void) { return 101; }
 
 const char *gdn_status_string(int status) {
     switch (status) {
@@ -143,6 +143,10 @@ int gdn_chunk_fwd(const gdn_problem *p, const void *q, const void *k, const void
     a.seq_info = reinterpret_cast<SeqInfo *>(ws + L.seq_off);
     a.chunk_info = reinterpret_cast<ChunkInfo *>(ws + L.chunk_off);
     a.status = status;
+    if (p->io_dtype == GDN_DT_BF16) {
+        a.ready = prefill_tc_ready_flags(ws + L.data_off, a.max_chunks, a.hv);
+        a.ready_count = a.max_chunks * a.hv;
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if ((st = cuda_status(launch_chunk_table(a, s)))) return st;
     if (p->io_dtype == GDN_DT_BF16) return cuda_status(launch_prefill_tc(a, ws + L.data_off, s));

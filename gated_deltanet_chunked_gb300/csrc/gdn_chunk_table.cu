@@ -22,6 +22,7 @@ __global__ void __launch_bounds__(kTableThreads) k_chunk_table(PrefillArgs a) {
     const int tid = threadIdx.x;
     const int N = a.num_seqs;
     if (tid == 0) bad = 0;
+    for (int i = tid; i < a.ready_count; i += kTableThreads) a.ready[i] = 0;
     __syncthreads();
     // 1) validate offsets: start at 0, non-decreasing, end at total_tokens
     if (a.cu) {

@@ -8,36 +8,33 @@
 //   O_c = scale [Gamma Q_c S_c + P_c V'_c],  P_c = Lower(Q K^T) * exp(gc_r - gc_i)
 //
 // A tcgen05 MMA round trip (issue, completion, wake-up) costs about 900 SM
-// cycles on this part whatever its size, so a serial walk with two dependent
-// products per chunk (W S, then K^T V') is latency-bound. Substituting the
-// state update into the next chunk's V' removes one of them:
+// cycles, so a serial walk with two dependent products per chunk (W S, then
+// K^T V') is latency-bound. Substituting the state update into the next
+// chunk's V' removes one of them:
 //   V'_{c+1} = U_{c+1} - (gamma_c W_{c+1}) S_c - G_c V'_c,
 //   G_c = W_{c+1} K_c^T diag(d_c)                    (chunk-parallel)
-// so (S_{c+1}, V'_{c+1}, O_c) all follow from (S_c, V'_c) in ONE batch of
-// MMAs. Stacking the two 64-row products that share a right operand gives
-// M = 128 MMAs (an M = 64 MMA runs at half the rate):
-//   D1 = [A_c+1 B ; 0] V_{c+1} + [-gamma_c W_{c+1} ; Gamma_c Q_c] S_c
-//        + [-G_c ; P_c] V'_c         rows 0..63 = V'_{c+1}, rows 64..127 = O_c/scale
-//   D2 = (diag(d_c) K_c)^T V'_c      S_{c+1} = gamma_c S_c + D2
-// The walk starts at a virtual step c = -1 with S_-1 = S0, V'_-1 = 0,
+// so (S_{c+1}, V'_{c+1}, O_c) all follow from (S_c, V'_c) in one batch of
+// MMAs. The walk starts at a virtual step c = -1 with S_-1 = S0, V'_-1 = 0,
 // gamma_-1 = 1 and G_-1 = 0, which yields V'_0 = U_0 - W_0 S0.
 //
-// k_chunk_prepare_tc (grid: chunk x v-head, all SMs): gate prefix sums,
-//   [K;Q] K^T in one M=128 MMA, the masked gated M and its unit-lower-
-//   triangular inverse by blocked (16x16) forward substitution in f32, then
-//   W_c and G_{c-1} on the tensor cores. Writes, per (chunk, v-head), bf16
-//   tiles already in the 128B-swizzled K-major layout the state kernel's
-//   MMAs read: A B, -gamma_{c-1} W_c, -G_{c-1}, P_c; and f32 gc, beta.
-// k_chunk_state_output_tc (grid: 64-wide dv tile x v-head x sequence): the
-//   serial walk. One producer warp (TMA for q/k/v tiles, bulk copies for the
-//   prepared tiles, two step buffers), one MMA warp, four math warps holding
-//   the f32 state tile S[128 x 64] in registers (thread t = row t).
+// prep_unit (one unit = chunk c x v-head h): gate prefix sums, [K;Q] K^T in
+//   one M=128 MMA, the masked gated M and its unit-lower-triangular inverse
+//   by blocked (16x16) substitution in f32, then W_c, U_c^T and K_{c-1} W_c^T
+//   on the tensor cores. It writes bf16 tiles in the 128B-swizzled layouts
+//   the walk's MMAs read (P_c, -gamma_{c-1} W_c, -K_{c-1} W_c^T, U_c^T), f32
+//   Gamma and d tables, then a ready flag.
+// state_walk (one walk = sequence x v-head): the serial walk, transposed so
+//   that dv is the MMA's M dimension; see the comment above it.
+// k_chunk_fused_tc runs both in one cooperative grid, one CTA per SM: a few
+//   CTAs walk while the others prepare the later chunks.
 //
 // Tensor-memory layouts: an M=128 accumulator keeps row m in lane m; an M=64
 // accumulator keeps row r in lane 32 (r / 16) + r % 16.
-// Every mbarrier wait is bounded; on timeout the CTA records GDN_ETIMEOUT,
-// stops, drains its outstanding copies (bounded), frees TMEM and returns.
+// Every mbarrier and flag wait is bounded; on timeout the CTA records
+// GDN_ETIMEOUT, stops, drains its outstanding copies (bounded) and returns.
 #include <string.h>
+
+#include <cmath>
 
 #include "gdn_common.cuh"
 #include "tc_ptx.cuh"
@@ -61,6 +58,7 @@ constexpr uint32_t kUnitBytes = 6 * kTile;  // 48 KiB
 struct TcWs {
     uint8_t *unit;  // [max_chunks][hv][kUnitBytes]
     float *gb;      // [max_chunks][hv][128]: Gamma_r = exp(gc_r) (r < 64), then d_i (i < 64)
+    int *ready;     // [max_chunks][hv]: 1 once the unit is written (zeroed by the chunk table)
 };
 
 __host__ __device__ inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -72,6 +70,8 @@ TcWs tc_carve(void *base, int max_chunks, int hv) {
     w.unit = reinterpret_cast<uint8_t *>(p);
     p += al256(units * kUnitBytes);
     w.gb = reinterpret_cast<float *>(p);
+    p += al256(units * 128 * sizeof(float));
+    w.ready = reinterpret_cast<int *>(p);
     return w;
 }
 
@@ -126,7 +126,7 @@ __device__ __forceinline__ void warp_scan64(float &a0, float &a1, int lane) {
 }
 
 // ===========================================================================
-// k_chunk_prepare_tc: one CTA per (chunk, v-head), 128 threads, 3 CTAs/SM
+// prep_unit: one (chunk, v-head) unit on a 128-thread engine
 // ===========================================================================
 constexpr int kPrepThreads = 128;
 
@@ -147,14 +147,18 @@ struct PrepSmem {
 };
 
 
-__global__ void __launch_bounds__(kPrepThreads, 3)
-k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm_q,
-                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
-    extern __shared__ uint8_t smraw[];
-    PrepSmem &s = *reinterpret_cast<PrepSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
-    const int c = blockIdx.x, h = blockIdx.y, hk = h / a.group;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (c >= *a.n_chunks) return;  // also a rejected chunk table (-1)
+// One unit (chunk c, v-head h) on a prepare engine: 128 threads (four
+// consecutive warps, so warp % 4 is the TMEM lane quarter) synchronised on
+// their own named barrier, with their own shared-memory slice and 128 TMEM
+// columns. ld_phase / mma_phase carry the engine's mbarrier phases from unit
+// to unit.
+__device__ __forceinline__ void prep_unit(const PrefillArgs &a, const TcWs &w, const CUtensorMap *tm_q,
+                                          const CUtensorMap *tm_k, const CUtensorMap *tm_v, PrepSmem &s,
+                                          uint32_t tmem, int bar_id, uint32_t &ld_phase, uint32_t &mma_phase, int c,
+                                          int h) {
+    const int hk = h / a.group;
+    const int tid = threadIdx.x & (kPrepThreads - 1), warp = tid >> 5, lane = tid & 31;
+    auto ebar = [&]() { named_bar_sync(bar_id, kPrepThreads); };
     const ChunkInfo ci = a.chunk_info[c];
     const int l = ci.len;
     const bool has_prev = ci.idx > 0;  // chunk c-1 belongs to the same sequence (and is full)
@@ -168,16 +172,11 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
     float *T = graw + 128;                          // [3][256] block products of the solve
 
     if (tid == 0) {
-        s.abort = 0;
-        mbar_init(&s.bar_load, 1);
-        mbar_init(&s.bar_v, 1);
-        mbar_init(&s.bar_mma, 1);
-        fence_mbar_init();
         mbar_arrive_expect_tx(&s.bar_load, (has_prev ? 6u : 4u) * kTile);
         for (int hf = 0; hf < 2; ++hf) {
-            tma_load_3d(s.KQ + hf * 2 * kTile, &tm_k, 64 * hf, hk, ci.start, &s.bar_load);
-            tma_load_3d(s.KQ + hf * 2 * kTile + kTile, &tm_q, 64 * hf, hk, ci.start, &s.bar_load);
-            if (has_prev) tma_load_3d(s.Kp + hf * kTile, &tm_k, 64 * hf, hk, prev_start, &s.bar_load);
+            tma_load_3d(s.KQ + hf * 2 * kTile, tm_k, 64 * hf, hk, ci.start, &s.bar_load);
+            tma_load_3d(s.KQ + hf * 2 * kTile + kTile, tm_q, 64 * hf, hk, ci.start, &s.bar_load);
+            if (has_prev) tma_load_3d(s.Kp + hf * kTile, tm_k, 64 * hf, hk, prev_start, &s.bar_load);
         }
     }
     // gates of this chunk and of the previous one (independent loads, issued
@@ -189,19 +188,13 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
         const int i = tid - 64;
         s.beta[i] = i < l ? a.beta[size_t(ci.start + i) * a.hv + h] : 0.f;
     }
-    if (warp == 0) {
-        tmem_alloc(&s.tmem, 128);
-        tmem_relinquish();
-    }
     tc_fence_before();
-    __syncthreads();
+    ebar();
     tc_fence_after();
-    const uint32_t tmem = s.tmem;
-    uint32_t mma_phase = 0;
 
     // [K;Q] K^T : M=128 (rows 0-63 K K^T, rows 64-127 Q K^T), N=64, K=128
     if (tid == 0) {
-        if (mbar_wait(&s.bar_load, 0)) {
+        if (mbar_wait(&s.bar_load, ld_phase)) {
             tc_fence_after();
             const uint32_t kq = smem_u32(s.KQ);
             const uint32_t id = idesc_bf16_f32(128, 64, false, false);
@@ -225,7 +218,7 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
         dst[2 * lane] = a0;
         dst[2 * lane + 1] = a1;
     }
-    __syncthreads();
+    ebar();
     if (has_prev) gprev = -exp_decay(s.gcp[63]);  // gamma_{c-1} = exp(sum of the gates of chunk c-1)
     // The state walk gets Gamma_r = exp(gc_r) and d_i = exp(gc_{l-1} - gc_i)
     // (zero for i >= l); the gates past l are zero, so gc_63 = gc_{l-1}.
@@ -243,7 +236,7 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
     // the Q slots are free: V_c goes there for U^T (needed only after the solve)
     if (tid == 0 && !s.abort) {
         mbar_arrive_expect_tx(&s.bar_v, 2 * kTile);
-        for (int hf = 0; hf < 2; ++hf) tma_load_3d(s.KQ + hf * 2 * kTile + kTile, &tm_v, 64 * hf, h, ci.start, &s.bar_v);
+        for (int hf = 0; hf < 2; ++hf) tma_load_3d(s.KQ + hf * 2 * kTile + kTile, tm_v, 64 * hf, h, ci.start, &s.bar_v);
     }
     // ---- M (rows 0-63: K K^T) and P (rows 64-127: Q K^T), one row per thread ----
     if (ok_kq) {
@@ -288,7 +281,7 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
         }
     }
     tc_fence_before();
-    __syncthreads();
+    ebar();
     if (tid < 64) s.gc[tid] = exp_decay(s.gc[tid]);  // gc -> gamma (read only by the A diag(beta gamma) step)
     // ---- A = (I + M)^-1, 16x16 blocks ----
 
@@ -318,7 +311,7 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
 #pragma unroll
         for (int ii = 0; ii < 16; ++ii) M[(16 * b + ii) * kFPitch + 16 * b + jj] = x[ii];
     }
-    __syncthreads();
+    ebar();
     // off-diagonal blocks by anti-diagonal levels, the blocks of a level in
     // parallel:  level 1: (1,0) (2,1) (3,2);  level 2: (2,0) (3,1);  level 3: (3,0)
     //   T_ij = sum_{k=j}^{i-1} L_ik X_kj,   X_ij = -X_ii T_ij
@@ -356,7 +349,7 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
                 }
                 *reinterpret_cast<float2 *>(&T[j * 256 + ii * 16 + jj]) = make_float2(t0, t1);
             }
-            __syncthreads();
+            ebar();
 #pragma unroll
             for (int j = 0; j < nb; ++j) {
                 const int i = j + lev;
@@ -376,7 +369,7 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
                 }
                 *reinterpret_cast<float2 *>(M + (16 * j + ii) * kFPitch + 16 * i + jj) = make_float2(-o0, -o1);
             }
-            __syncthreads();
+            ebar();
         }
     }
     // ---- A diag(beta) and A diag(beta gamma) -> bf16 smem operands ----
@@ -397,7 +390,7 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
             xs[k2][0] = x0.x; xs[k2][1] = x0.y; xs[k2][2] = x0.z; xs[k2][3] = x0.w;
             xs[k2][4] = x1.x; xs[k2][5] = x1.y; xs[k2][6] = x1.z; xs[k2][7] = x1.w;
         }
-        __syncthreads();
+        ebar();
 #pragma unroll
         for (int k2 = 0; k2 < 4; ++k2) {
             const int p = tid + kPrepThreads * k2, i = p >> 3, ch = p & 7;
@@ -414,7 +407,7 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
     }
     fence_proxy_async_smem();
     tc_fence_before();
-    __syncthreads();
+    ebar();
     // ---- W_c = Ag K_c : M=64, N=128 (d), K=64 (j); K tile read MN-major ----
     if (tid == 0 && !s.abort) {
         tc_fence_after();
@@ -426,7 +419,7 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
                      t > 0);
         mma_commit(&s.bar_mma);
     }
-    __syncthreads();
+    ebar();
     if (!s.abort && !mbar_wait(&s.bar_mma, mma_phase)) s.abort = 1;
     mma_phase ^= 1;
     tc_fence_after();
@@ -454,7 +447,7 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
     }
     fence_proxy_async_smem();
     tc_fence_before();
-    __syncthreads();
+    ebar();
     if (tid == 0) {  // whole 8 KiB tiles: one bulk copy each instead of scattered 16-byte stores
         bulk_store(uo + kUnitW, s.Ag, kTile);
         bulk_store(uo + kUnitW + kTile, wst1, kTile);
@@ -463,7 +456,7 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
     // ---- U_c^T = V_c^T (A diag(beta))^T : M=128 (e), N=64 (i), K=64 (j),
     //      V tile read as an MN-major A;  K_{c-1} W_c^T : M=64 (t), N=64 (i), K=128
     if (tid == 0 && !s.abort) {
-        if (mbar_wait(&s.bar_v, 0)) {
+        if (mbar_wait(&s.bar_v, ld_phase)) {
             tc_fence_after();
             const uint32_t kq = smem_u32(s.KQ), ab = smem_u32(Ab);
             const uint32_t idu = idesc_bf16_f32(128, 64, true, false);
@@ -484,7 +477,7 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
             s.abort = 1;
         }
     }
-    __syncthreads();
+    ebar();
     const bool ok_u = __all_sync(0xffffffffu, !s.abort && mbar_wait(&s.bar_mma, mma_phase));
     if (!ok_u) s.abort = 1;
     mma_phase ^= 1;
@@ -521,7 +514,7 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
             reinterpret_cast<uint4 *>(uo + kUnitG)[p] = make_uint4(0, 0, 0, 0);
     }
     fence_proxy_async_smem();
-    __syncthreads();
+    ebar();
     if (tid == 0) {
         if (ok_u) {
             bulk_store(uo + kUnitU, s.KQ + kTile, kTile);
@@ -533,16 +526,23 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
     }
     if (s.abort && tid == 0) {
         record_status(a.status, GDN_ETIMEOUT);
-        mbar_wait(&s.bar_load, 0, 100000000ull);  // bounded drain of the tile copies
-        mbar_wait(&s.bar_v, 0, 100000000ull);
+        mbar_wait(&s.bar_load, ld_phase, 100000000ull);  // bounded drain of the tile copies
+        mbar_wait(&s.bar_v, ld_phase, 100000000ull);
     }
+    ld_phase ^= 1;
+    // publish the unit: the plain stores of every engine thread are ordered
+    // before the flag by the barrier, the bulk copies completed above
     tc_fence_before();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 128);
+    ebar();
+    if (tid == 0 && !s.abort) {
+        fence_proxy_async_global();
+        __threadfence();
+        st_release_gpu(w.ready + unit, 1);
+    }
 }
 
 // ===========================================================================
-// k_chunk_state_output_tc: one CTA per (sequence, v-head), 320 threads
+// state_walk: one (sequence, v-head) walk on 10 warps
 // ===========================================================================
 // The walk runs transposed, with dv (e) as the MMA's M dimension so that the
 // whole 128-wide state of a head is one M=128 accumulator and the operands the
@@ -554,7 +554,7 @@ k_chunk_prepare_tc(PrefillArgs a, TcWs w, const __grid_constant__ CUtensorMap tm
 //   (b) X_c P_c^T                                                             N=64,  K=64
 // then V'^T_{c+1} = U^T_{c+1} + partial and O_c^T = scale (Sigma_c Q_c^T Gamma_c + X_c P_c^T).
 constexpr int kMathThreads = 256;   // 8 warps: lane quarter (warp % 4) x column half (warp / 4)
-constexpr int kStateThreads = 320;  // + copy warp (lane 0: MMA operands, lane 1: epilogue data) + MMA warp
+constexpr int kStateThreads = 320;  // + copy warp (one polling thread) + MMA warp
 constexpr int kCopyWarp = 8, kMmaWarp = 9;
 
 // tensor-memory columns (512 allocated)
@@ -587,42 +587,26 @@ struct StateSmem {
     int abort;
 };
 
-struct StateArgs {
-    PrefillArgs a;
-    TcWs w;
-};
-
-// dynamic shared memory per block is capped at 227 KiB; one more KiB is
-// requested to align the base to 1024 bytes
-static_assert(sizeof(StateSmem) + 1024 <= 227 * 1024, "state kernel shared memory");
 static_assert(sizeof(BStage) % 1024 == 0 && sizeof(MStage) % 1024 == 0, "stages keep the swizzle alignment");
-// three CTAs per SM: 228 KiB per SM, 1 KiB reserved per CTA, 1 KiB alignment slack
-static_assert(3 * (sizeof(PrepSmem) + 2048) <= 228 * 1024, "three prepare CTAs per SM");
 
 __device__ __forceinline__ void pack_row(const float *x, uint32_t *r, int n2) {
 #pragma unroll
     for (int j = 0; j < n2; ++j) r[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]);
 }
 
-__global__ void __launch_bounds__(kStateThreads, 1)
-k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
-                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_o) {
-    extern __shared__ uint8_t smraw[];
-    StateSmem &s = *reinterpret_cast<StateSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
-    const PrefillArgs &a = sa.a;
-    const TcWs &w = sa.w;
-    const int n = blockIdx.x, h = blockIdx.y, hk = h / a.group;
+// One walk (sequence n, v-head h). Every thread of the CTA calls it (warps
+// past the MMA warp only join the barriers); the caller has zeroed the
+// shared memory once and holds 512 TMEM columns at `tmem`.
+__device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, const CUtensorMap *tm_q,
+                                           const CUtensorMap *tm_k, const CUtensorMap *tm_o, StateSmem &s,
+                                           uint32_t tmem, int n, int h) {
+    const int hk = h / a.group;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (*a.n_chunks < 0) return;  // the chunk table rejected cu_seqlens
     const SeqInfo si = a.seq_info[n];
     const int nc = si.num_chunks;
     const size_t sbase = (size_t(n) * a.hv + h) * kHeadDim * kHeadDim;
 
-    // zero every operand buffer once: regions a step does not load must hold
-    // finite values (their products land in columns that are discarded)
-    for (uint32_t o = tid * 16; o < sizeof(StateSmem) - 64; o += kStateThreads * 16)
-        *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(&s) + o) = make_uint4(0, 0, 0, 0);
-    __syncthreads();
+    __syncthreads();  // the previous walk of this CTA is over: barriers may be re-armed
     if (tid == 0) {
         s.abort = 0;
         for (int b = 0; b < 2; ++b) {
@@ -638,14 +622,9 @@ k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
         mbar_init(&s.o_free, kMathThreads);
         fence_mbar_init();
     }
-    if (warp == 0) {
-        tmem_alloc(&s.tmem, 512);
-        tmem_relinquish();
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = s.tmem;
 
     if (warp == kCopyWarp) {
         // --------------------------- copy thread ----------------------------
@@ -654,15 +633,27 @@ k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
         // next operand loads (two spinning lanes of one warp would starve
         // each other)
         if (lane == 0 && nc > 0) {
-            prefetch_tensormap(&tm_q);
-            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(tm_q);
+            prefetch_tensormap(tm_k);
             int cb = -1, cm = -1;  // next step whose operands / epilogue data are loaded
+            // chunks 0 .. known of this walk are written by the prepare engines
+            // (their flags acquired, so their stores are visible to the copies)
+            int known = -1;
+            auto units_ready = [&](int upto) {  // chunks 0 .. upto of this walk
+                while (known < upto) {
+                    if (!ld_acquire_gpu(w.ready + size_t(si.first_chunk + known + 1) * a.hv + h)) return false;
+                    ++known;
+                    fence_proxy_async_global();  // the bulk copies read what the flag published
+                }
+                return true;
+            };
             uint64_t t0 = globaltimer_ns();
             while ((cb < nc || cm < nc) && !s.abort) {
                 bool progressed = false;
                 if (cb < nc) {
                     const int c = cb, b = (c + 1) & 1, use = (c + 1) >> 1;
-                    if (use == 0 || mbar_try_wait(&s.emptyB[b], (use - 1) & 1)) {
+                    if (units_ready(min(c + 1, nc - 1)) &&
+                        (use == 0 || mbar_try_wait(&s.emptyB[b], (use - 1) & 1))) {
                         const bool cur = c >= 0, nxt = c + 1 < nc;
                         BStage &B = s.bs[b];
                         mbar_arrive_expect_tx(&s.fullB[b], (cur ? 5 * kTile : 0) + (nxt ? 3 * kTile : 0));
@@ -670,8 +661,8 @@ k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
                             const int start = si.start + kChunk * c;
                             const uint8_t *uc = w.unit + (size_t(si.first_chunk + c) * a.hv + h) * kUnitBytes;
                             for (int hf = 0; hf < 2; ++hf) {
-                                tma_load_3d(B.B1 + hf * kTile, &tm_k, 64 * hf, hk, start, &s.fullB[b]);
-                                tma_load_3d(B.B2 + hf * 2 * kTile + kTile, &tm_q, 64 * hf, hk, start, &s.fullB[b]);
+                                tma_load_3d(B.B1 + hf * kTile, tm_k, 64 * hf, hk, start, &s.fullB[b]);
+                                tma_load_3d(B.B2 + hf * 2 * kTile + kTile, tm_q, 64 * hf, hk, start, &s.fullB[b]);
                             }
                             bulk_load(B.Pc, uc + kUnitP, kTile, &s.fullB[b]);
                         }
@@ -687,7 +678,8 @@ k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
                 }
                 if (cm < nc) {
                     const int c = cm, b = (c + 1) & 1, use = (c + 1) >> 1;
-                    if (use == 0 || mbar_try_wait(&s.emptyM[b], (use - 1) & 1)) {
+                    if (units_ready(min(c + 1, nc - 1)) &&
+                        (use == 0 || mbar_try_wait(&s.emptyM[b], (use - 1) & 1))) {
                         const bool cur = c >= 0, nxt = c + 1 < nc;
                         MStage &M = s.ms[b];
                         mbar_arrive_expect_tx(&s.fullM[b], (cur ? 512 : 0) + (nxt ? 2 * kTile + 512 : 0));
@@ -768,8 +760,15 @@ k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
                 }
                 mma_commit(&s.emptyB[b]);
             }
+            // the last arrivals on the operand-release barriers come from MMA
+            // completion: wait for them so that nothing lands after the next
+            // walk has re-armed the barriers
+            for (int b = 0; b < 2; ++b) {
+                const int uses = (nc + 2 - b) >> 1;  // steps -1 .. nc-1 that used stage b
+                if (uses > 0) mbar_wait(&s.emptyB[b], (uses - 1) & 1, 100000000ull);
+            }
         }
-    } else {
+    } else if (warp < kMathThreads / 32) {
         // --------------------------- math warps ----------------------------
         const int lq = warp & 3, ch = warp >> 2;  // TMEM lane quarter, column half
         const int e = 32 * lq + lane;             // dv index = TMEM lane
@@ -917,7 +916,7 @@ k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_3d(&tm_o, 32 * lq, h, row0, blk);
+                        tma_store_3d(tm_o, 32 * lq, h, row0, blk);
                         bulk_commit_group();
                     }
                 } else {
@@ -933,8 +932,84 @@ k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
         }
         if (lane == 0) bulk_wait_group_all();  // output stores complete before the CTA exits
     }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
     if (s.abort && tid == 0) record_status(a.status, GDN_ETIMEOUT);
+}
+
+// ===========================================================================
+// k_chunk_fused_tc: prepare engines and state walks in one co-resident grid
+// ===========================================================================
+// One CTA per SM (cooperative launch, so every CTA is resident at once).
+// CTAs 0 .. n_state-1 run state walks, one after another in sequence order;
+// the others run three prepare engines each, which take the units in
+// chunk-major order and never wait on anything but their own copies. A walk
+// waits (bounded) on the ready flag of each unit it loads, so the walks run
+// while later chunks are still being prepared.
+constexpr int kFusedThreads = 384;  // three 4-warp engines, or one walk (8 math + copy + MMA warps)
+constexpr int kEngines = kFusedThreads / kPrepThreads;
+
+struct FusedArgs {
+    PrefillArgs a;
+    TcWs w;
+    int n_state;  // CTAs that walk; the rest prepare
+};
+
+union FusedSmem {
+    PrepSmem prep[kEngines];
+    StateSmem state;
+};
+// dynamic shared memory per block is capped at 227 KiB; one more KiB is
+// requested to align the base to 1024 bytes
+static_assert(sizeof(FusedSmem) + 1024 <= 227 * 1024, "fused kernel shared memory");
+static_assert(sizeof(PrepSmem) % 1024 == 0, "engine slices keep the swizzle alignment");
+
+__global__ void __launch_bounds__(kFusedThreads, 1)
+k_chunk_fused_tc(FusedArgs fa, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o) {
+    extern __shared__ uint8_t smraw[];
+    __shared__ uint32_t tmem_slot;
+    FusedSmem &sm = *reinterpret_cast<FusedSmem *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    const PrefillArgs &a = fa.a;
+    const TcWs &w = fa.w;
+    const int nch = *a.n_chunks;
+    if (nch < 0) return;  // the chunk table rejected cu_seqlens (uniform over the grid)
+    const int tid = threadIdx.x, warp = tid >> 5;
+    if (warp == 0) {
+        tmem_alloc(&tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    if (int(blockIdx.x) < fa.n_state) {
+        StateSmem &s = sm.state;
+        // zero once: operand regions a step does not load must hold finite
+        // values (their products land in columns that are discarded)
+        for (uint32_t o = tid * 16; o < sizeof(StateSmem) - 64; o += kFusedThreads * 16)
+            *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(&s) + o) = make_uint4(0, 0, 0, 0);
+        const int walks = a.num_seqs * a.hv;
+        for (int wk = blockIdx.x; wk < walks; wk += fa.n_state)
+            state_walk(a, w, &tm_q, &tm_k, &tm_o, s, tmem, wk / a.hv, wk % a.hv);
+    } else {
+        const int e = warp / (kPrepThreads / 32);
+        PrepSmem &s = sm.prep[e];
+        if ((tid & (kPrepThreads - 1)) == 0) {
+            s.abort = 0;
+            mbar_init(&s.bar_load, 1);
+            mbar_init(&s.bar_v, 1);
+            mbar_init(&s.bar_mma, 1);
+            fence_mbar_init();
+        }
+        __syncthreads();
+        uint32_t ld_phase = 0, mma_phase = 0;
+        const int units = nch * a.hv;
+        const int stride = (int(gridDim.x) - fa.n_state) * kEngines;
+        for (int u = (int(blockIdx.x) - fa.n_state) * kEngines + e; u < units && !s.abort; u += stride)
+            prep_unit(a, w, &tm_q, &tm_k, &tm_v, s, tmem + 128 * e, 1 + e, ld_phase, mma_phase, u / a.hv, u % a.hv);
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 512);
@@ -944,7 +1019,30 @@ k_chunk_state_output_tc(StateArgs sa, const __grid_constant__ CUtensorMap tm_q,
 
 size_t prefill_tc_workspace(int max_chunks, int hv) {
     const size_t units = size_t(max_chunks) * hv;
-    return al256(units * kUnitBytes) + al256(units * 128 * sizeof(float));
+    return al256(units * kUnitBytes) + al256(units * 128 * sizeof(float)) + al256(units * sizeof(int));
+}
+
+int *prefill_tc_ready_flags(void *ws_data, int max_chunks, int hv) { return tc_carve(ws_data, max_chunks, hv).ready; }
+
+// CTAs that walk: the split that minimises the larger of the two estimated
+// times (a walk step ~1.7 us, an engine unit ~17 us, measured at T=4096),
+// with the chunks of a sequence estimated from the mean length.
+static int state_ctas(const PrefillArgs &a, int ctas) {
+    const int walks = a.num_seqs * a.hv;
+    const double steps = double(a.total_tokens) / (double(kChunk) * (a.num_seqs > 0 ? a.num_seqs : 1)) + 2.0;
+    const double units = double(a.max_chunks) * a.hv;
+    int best = 1;
+    double best_t = 1e300;
+    for (int n = 1; n < ctas && n <= walks; ++n) {
+        const double t_walk = double((walks + n - 1) / n) * steps * 1.7;
+        const double t_prep = std::ceil(units / (double(ctas - n) * kEngines)) * 17.0;
+        const double t = t_walk > t_prep ? t_walk : t_prep;
+        if (t < best_t) {
+            best_t = t;
+            best = n;
+        }
+    }
+    return best;
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs &a, void *ws_data, cudaStream_t s) {
@@ -955,8 +1053,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, void *ws_data, cudaStream_t 
     memset(&tk, 0, sizeof(tk));
     memset(&tv, 0, sizeof(tv));
     memset(&to, 0, sizeof(to));
-    // with no tokens every sequence is empty: the state kernel only copies
-    // S0 to the final state and never touches the (then unset) tensor maps
+    // with no tokens every sequence is empty: the walks only copy S0 to the
+    // final state and never touch the (then unset) tensor maps
     if (T > 0 &&
         (!make_tmap_bf16_3d(&tq, a.q, kHeadDim, a.hq, T, kHeadDim * 2, uint64_t(a.hq) * kHeadDim * 2, 64, 1, 64) ||
          !make_tmap_bf16_3d(&tk, a.k, kHeadDim, a.hq, T, kHeadDim * 2, uint64_t(a.hq) * kHeadDim * 2, 64, 1, 64) ||
@@ -964,24 +1062,21 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, void *ws_data, cudaStream_t 
          !make_tmap_bf16_3d(&to, a.out, kHeadDim, a.hv, T, kHeadDim * 2, uint64_t(a.hv) * kHeadDim * 2, 32, 1, 32,
                             false)))
         return cudaErrorInvalidValue;
-    const size_t prep_smem = sizeof(PrepSmem) + 1024;
-    const size_t state_smem = sizeof(StateSmem) + 1024;
+    const size_t smem = sizeof(FusedSmem) + 1024;
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(k_chunk_prepare_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, int(prep_smem))))
+    if ((e = cudaFuncSetAttribute(k_chunk_fused_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem))))
         return e;
-    if ((e = cudaFuncSetAttribute(k_chunk_state_output_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  int(state_smem))))
-        return e;
-    if (a.max_chunks > 0 && T > 0) {
-        LaunchScope scope(GDN_K_CHUNK_PREPARE_TC, s);
-        k_chunk_prepare_tc<<<dim3(a.max_chunks, a.hv), kPrepThreads, prep_smem, s>>>(a, w, tq, tk, tv);
-    }
-    if ((e = cudaGetLastError())) return e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) || (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
+    if (sms < 2) return cudaErrorInvalidConfiguration;
+    FusedArgs fa{a, w, state_ctas(a, sms)};
+    void *args[] = {&fa, &tq, &tk, &tv, &to};
     {
-        LaunchScope scope(GDN_K_STATE_OUTPUT_TC, s);
-        StateArgs sa{a, w};
-        k_chunk_state_output_tc<<<dim3(a.num_seqs, a.hv), kStateThreads, state_smem, s>>>(sa, tq, tk, to);
+        LaunchScope scope(GDN_K_CHUNK_FUSED_TC, s);
+        e = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(k_chunk_fused_tc), dim3(sms),
+                                        dim3(kFusedThreads), args, smem, s);
     }
+    if (e) return e;
     return cudaGetLastError();
 }
 

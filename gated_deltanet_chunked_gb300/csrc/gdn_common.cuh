@@ -46,6 +46,8 @@ struct PrefillArgs {
     SeqInfo *seq_info;  // [num_seqs]
     ChunkInfo *chunk_info;  // [max_chunks]
     int *status;  // device status word
+    int *ready;       // per-unit ready flags of the tensor-core path (zeroed by the chunk table), or null
+    int ready_count;
 };
 
 __device__ __forceinline__ void record_status(int *status, int code) {
@@ -86,6 +88,7 @@ cudaError_t launch_chunk_table(const PrefillArgs &a, cudaStream_t s);
 cudaError_t launch_prefill_simt(const PrefillArgs &a, void *ws_data, cudaStream_t s);
 size_t prefill_simt_workspace(int max_chunks, int hv);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, void *ws_data, cudaStream_t s);
+int *prefill_tc_ready_flags(void *ws_data, int max_chunks, int hv);
 size_t prefill_tc_workspace(int max_chunks, int hv);
 cudaError_t launch_recurrent_step(const gdn_problem &p, const void *q, const void *k, const void *v,
                                   const float *g, const float *beta, float scale, float *state,

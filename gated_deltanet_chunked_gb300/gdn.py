@@ -25,7 +25,7 @@ GDN_DT_F32, GDN_DT_BF16 = 0, 1
 SYMBOLS = ("gdn_chunk_fwd", "gdn_chunk_fwd_workspace_size", "gdn_recurrent_step", "gdn_read_device_status",
            "gdn_status_string", "gdn_version", "gdn_profile_enable", "gdn_profile_collect", "gdn_kernel_name",
            "gdn_chunk_fwd_noalloc")
-GDN_K_COUNT = 7
+GDN_K_COUNT = 6
 
 
 class GdnProblem(ctypes.Structure):

@@ -181,9 +181,8 @@ typedef enum gdn_kernel {
     GDN_K_STATE_SIMT = 2,         /* f32: sequential state pass */
     GDN_K_OUTPUT_SIMT = 3,        /* f32: chunk output */
     GDN_K_RECURRENT_STEP = 4,     /* decode step */
-    GDN_K_CHUNK_PREPARE_TC = 5,   /* bf16: gate cumsum + KK^T solve (tensor cores) */
-    GDN_K_STATE_OUTPUT_TC = 6,    /* bf16: W, U, state pass and output (tensor cores) */
-    GDN_K_COUNT = 7
+    GDN_K_CHUNK_FUSED_TC = 5,     /* bf16: chunk preparation and state walk, one co-resident grid (tensor cores) */
+    GDN_K_COUNT = 6
 } gdn_kernel;
 
 /* Turns per-kernel CUDA-event timing on (non-zero) or off for every later
