@@ -53,7 +53,8 @@ constexpr uint32_t kUnitP = 0;              // P_c                  [r][j]  64 r
 constexpr uint32_t kUnitW = kTile;          // -gamma_{c-1} W_c     [i][d]  64 rows, two d-halves
 constexpr uint32_t kUnitG = 3 * kTile;      // -K_{c-1} W_c^T       [t][i]  64 rows
 constexpr uint32_t kUnitU = 4 * kTile;      // U_c^T = (A B V)^T    [e][i] 128 rows
-constexpr uint32_t kUnitBytes = 6 * kTile;  // 48 KiB
+constexpr uint32_t kUnitQ = 6 * kTile;      // scale Gamma Q_c      [r][d]  64 rows, two d-halves
+constexpr uint32_t kUnitBytes = 8 * kTile;  // 64 KiB
 
 struct TcWs {
     uint8_t *unit;  // [max_chunks][hv][kUnitBytes]
@@ -228,6 +229,22 @@ __device__ __forceinline__ void prep_unit(const PrefillArgs &a, const TcWs &w, c
         const int i = tid - 64;
         w.gb[unit * 128 + 64 + i] = i < l ? exp_decay(s.gc[63] - s.gc[i]) : 0.f;
     }
+    // scale Gamma_r Q_r for the walk's output product, while [K;Q]K^T runs
+    // (both only read the Q tile). A row scale commutes with the swizzle
+    // inside the row, so the copy is linear: thread p moves bytes 16p..16p+15
+    // of each 8 KiB half, and every warp writes 512 contiguous bytes.
+    if (mbar_wait(&s.bar_load, ld_phase)) {
+#pragma unroll 2
+        for (int k2 = 0; k2 < 8; ++k2) {
+            const int p = tid + kPrepThreads * k2, hf = p >> 9, o16 = p & 511, r = o16 >> 3;
+            float x[8];
+            unpack8(*reinterpret_cast<const uint4 *>(s.KQ + hf * 2 * kTile + kTile + 16 * o16), x);
+            const float f = a.scale * exp_decay(s.gc[r]);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[j] *= f;
+            *reinterpret_cast<uint4 *>(uo + kUnitQ + hf * kTile + 16 * o16) = pack8(x);
+        }
+    }
     // warp-uniform outcome: the tcgen05 loads below are .sync.aligned
     const bool ok_kq = __all_sync(0xffffffffu, !s.abort && mbar_wait(&s.bar_mma, mma_phase));
     if (!ok_kq) s.abort = 1;
@@ -253,7 +270,7 @@ __device__ __forceinline__ void prep_unit(const PrefillArgs &a, const TcWs &w, c
         const int rmax = (tid & 32) + 31;  // last row held by this warp
         const float gr = s.gc[r];
         const bool live = r < l;
-        const float sr = warp < 2 ? s.beta[r] : 1.f;  // M rows carry beta_r
+        const float sr = warp < 2 ? s.beta[r] : a.scale;  // M rows carry beta_r, P rows the output scale
         const int strict = warp < 2 ? 1 : 0;          // M is strictly lower, P includes the diagonal
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
@@ -548,20 +565,21 @@ __device__ __forceinline__ void prep_unit(const PrefillArgs &a, const TcWs &w, c
 // whole 128-wide state of a head is one M=128 accumulator and the operands the
 // math warps produce each step (Sigma = S^T and X = V'^T) are written straight
 // into tensor memory as the A operands of the next step's MMAs:
-//   (c) [V'^T partial | Sigma_c Q_c^T] = Sigma_c [-gamma_c W_{c+1} ; Q_c]^T     N=128, K=128
+//   (c) [V'^T partial | O_c^T part] = Sigma_c [-gamma_c W_{c+1} ; s Gamma_c Q_c]^T  N=128, K=128
 //   (a) [Sigma_{c+1} | V'^T partial] += X'_c [K_c | -K_c W_{c+1}^T]           N=192, K=64
 //       with X'_c = X_c diag(d_c) and the Sigma columns preloaded with gamma_c Sigma_c
-//   (b) X_c P_c^T                                                             N=64,  K=64
-// then V'^T_{c+1} = U^T_{c+1} + partial and O_c^T = scale (Sigma_c Q_c^T Gamma_c + X_c P_c^T).
-constexpr int kMathThreads = 256;   // 8 warps: lane quarter (warp % 4) x column half (warp / 4)
-constexpr int kStateThreads = 320;  // + copy warp (one polling thread) + MMA warp
+//   (b) O_c^T part += X_c (s P_c)^T                                          N=64,  K=64
+// then V'^T_{c+1} = U^T_{c+1} + partial, and the O columns hold
+// O_c^T = s (Sigma_c (Gamma_c Q_c)^T + X_c P_c^T) (s the output scale, folded
+// into the prepared Q and P tiles).
+constexpr int kMathThreads = 256;   // 8 warps: lane quarter (warp % 4) x column half (warp / 4),
+                                    // then a copy warp (one polling thread) and an MMA warp
 constexpr int kCopyWarp = 8, kMmaWarp = 9;
 
 // tensor-memory columns (512 allocated)
 constexpr uint32_t kTmSig = 0;    // Sigma accumulator f32 [e][k], 128 columns
 constexpr uint32_t kTmV = 128;    // V'^T_{c+1} partial, 64 columns
-constexpr uint32_t kTmSQ = 192;   // Sigma_c Q_c^T, 64 columns
-constexpr uint32_t kTmXP = 256;   // X_c P_c^T, 64 columns
+constexpr uint32_t kTmO = 192;    // O_c^T, 64 columns
 constexpr uint32_t kTmSA = 320;   // Sigma_c bf16 A operand (K = 128), 64 columns
 constexpr uint32_t kTmXA = 384;   // X_c bf16 A operand (K = 64), two buffers of 32 columns
 constexpr uint32_t kTmXdA = 448;  // X'_c bf16 A operand, 32 columns
@@ -569,12 +587,12 @@ constexpr uint32_t kTmXdA = 448;  // X'_c bf16 A operand, 32 columns
 struct BStage {                           // MMA operands of one step
     alignas(1024) uint8_t B1[3 * kTile];  // [K_c (two d-halves) | -K_c W_{c+1}^T], MN-major rows t
     alignas(1024) uint8_t Pc[kTile];      // P_c [r][j], K-major
-    alignas(1024) uint8_t B2[4 * kTile];  // per d-half: [-gamma_c W_{c+1} ; Q_c] rows, K-major
+    alignas(1024) uint8_t B2[4 * kTile];  // per d-half: [-gamma_c W_{c+1} ; s Gamma_c Q_c] rows, K-major
 };
 struct MStage {                           // what the math warps read in one step
     alignas(1024) uint8_t Ut[2 * kTile];  // U^T_{c+1} [e][i]
-    float gbc[128];                       // Gamma_c, d_c
     float gbn[128];                       // Gamma_{c+1}, d_{c+1}
+    float pad[128];
 };
 struct StateSmem {
     BStage bs[2];
@@ -582,7 +600,7 @@ struct StateSmem {
     // per math warp, two staging buffers of its 32 x 32 bf16 output block
     // (rows r, 64-byte rows of e) for TMA stores
     alignas(1024) uint8_t Ost[8][2][2048];
-    uint64_t fullB[2], emptyB[2], fullM[2], emptyM[2], ready_s, ready_x, mma, mma_o, o_free;
+    uint64_t fullB[2], emptyB[2], fullM[2], emptyM[2], ready_s, ready_x, mma, mma_o;
     uint32_t tmem;
     int abort;
 };
@@ -619,7 +637,6 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
         mbar_init(&s.ready_x, kMathThreads);
         mbar_init(&s.mma, 1);
         mbar_init(&s.mma_o, 1);
-        mbar_init(&s.o_free, kMathThreads);
         fence_mbar_init();
     }
     tc_fence_before();
@@ -633,7 +650,6 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
         // next operand loads (two spinning lanes of one warp would starve
         // each other)
         if (lane == 0 && nc > 0) {
-            prefetch_tensormap(tm_q);
             prefetch_tensormap(tm_k);
             int cb = -1, cm = -1;  // next step whose operands / epilogue data are loaded
             // chunks 0 .. known of this walk are written by the prepare engines
@@ -662,7 +678,7 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
                             const uint8_t *uc = w.unit + (size_t(si.first_chunk + c) * a.hv + h) * kUnitBytes;
                             for (int hf = 0; hf < 2; ++hf) {
                                 tma_load_3d(B.B1 + hf * kTile, tm_k, 64 * hf, hk, start, &s.fullB[b]);
-                                tma_load_3d(B.B2 + hf * 2 * kTile + kTile, tm_q, 64 * hf, hk, start, &s.fullB[b]);
+                                bulk_load(B.B2 + hf * 2 * kTile + kTile, uc + kUnitQ + hf * kTile, kTile, &s.fullB[b]);
                             }
                             bulk_load(B.Pc, uc + kUnitP, kTile, &s.fullB[b]);
                         }
@@ -680,10 +696,9 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
                     const int c = cm, b = (c + 1) & 1, use = (c + 1) >> 1;
                     if (units_ready(min(c + 1, nc - 1)) &&
                         (use == 0 || mbar_try_wait(&s.emptyM[b], (use - 1) & 1))) {
-                        const bool cur = c >= 0, nxt = c + 1 < nc;
+                        const bool nxt = c + 1 < nc;
                         MStage &M = s.ms[b];
-                        mbar_arrive_expect_tx(&s.fullM[b], (cur ? 512 : 0) + (nxt ? 2 * kTile + 512 : 0));
-                        if (cur) bulk_load(M.gbc, w.gb + (size_t(si.first_chunk + c) * a.hv + h) * 128, 512, &s.fullM[b]);
+                        mbar_arrive_expect_tx(&s.fullM[b], nxt ? 2 * kTile + 512 : 0);
                         if (nxt) {
                             const size_t un = size_t(si.first_chunk + c + 1) * a.hv + h;
                             bulk_load(M.Ut, w.unit + un * kUnitBytes + kUnitU, 2 * kTile, &s.fullM[b]);
@@ -747,15 +762,10 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
                     mma_bf16_ts(tmem + kTmSig, tmem + kTmXdA + 8 * t, dB1 + ob + ((2048 * t) >> 4), id_a, 1);
                 mma_commit(&s.mma);
                 if (c >= 0) {
-                    if (c >= 1 && !mbar_wait(&s.o_free, (c - 1) & 1)) {
-                        s.abort = 1;
-                        break;
-                    }
-                    tc_fence_after();
                     const uint32_t xa = kTmXA + 32 * ((c + 1) & 1);
 #pragma unroll
-                    for (int t = 0; t < 4; ++t)  // (b) X_c P_c^T
-                        mma_bf16_ts(tmem + kTmXP, tmem + xa + 8 * t, dPc + ob + ((32 * t) >> 4), id_b, t > 0);
+                    for (int t = 0; t < 4; ++t)  // (b) O_c^T += X_c (s P_c)^T, onto the output part of (c)
+                        mma_bf16_ts(tmem + kTmO, tmem + xa + 8 * t, dPc + ob + ((32 * t) >> 4), id_b, 1);
                     mma_commit(&s.mma_o);
                 }
                 mma_commit(&s.emptyB[b]);
@@ -812,14 +822,23 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
             }
             tc_fence_after();
             const MStage &M = s.ms[b];
-            float sq[32], x[32];
-            tmem_ld32(tmem + lrow + kTmSQ + 32 * ch, sq);
+            // O_c (from the output columns, complete once (b) is) is read
+            // before the next step's (c) may overwrite those columns
+            auto read_o = [&](float *o) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&s.mma_o, c & 1))) return false;
+                tc_fence_after();
+                tmem_ld32(tmem + lrow + kTmO + 32 * ch, o);
+                tmem_ld_wait();
+                return true;
+            };
+            float o[32], x[32];
+            bool ok = true;
             if (c + 1 < nc) {
                 // phase 1: Sigma_{c+1} as the bf16 A operand of the next (c), and
                 // gamma_{c+1} Sigma_{c+1} back into the accumulator for the next (a),
                 // read in two halves of 32 columns. Done while the tensor pipe is
                 // idle: TMEM stores slow down MMAs that run beside them. The next (c)
-                // overwrites the V'^T partial and Sigma Q^T columns, so both are read
+                // overwrites the V'^T partial and output columns, so both are read
                 // before it may start.
                 const float gam = M.gbn[63];  // gamma_{c+1}
                 tmem_ld32(tmem + lrow + kTmV + 32 * ch, x);
@@ -835,6 +854,7 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
                     for (int j = 0; j < 32; ++j) v[j] *= gam;
                     tmem_st32(tmem + lrow + kTmSig + 64 * ch + 32 * hq, reinterpret_cast<const uint32_t *>(v));
                 }
+                if (c >= 0) ok = read_o(o);
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(&s.ready_s);
@@ -871,28 +891,14 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
                     for (int j = 0; j < 64; ++j)
                         a.final_state[sbase + size_t(64 * ch + j) * kHeadDim + e] = v[j];
                 }
+                if (c >= 0) ok = read_o(o);
+            }
+            if (!ok) {
+                s.abort = 1;
+                break;
             }
             if (c >= 0) {
                 // O_c rows r = 32 ch + j, column e
-                if (!__all_sync(0xffffffffu, mbar_wait(&s.mma_o, c & 1))) {
-                    s.abort = 1;
-                    break;
-                }
-                tc_fence_after();
-                float o[32];
-                tmem_ld32(tmem + lrow + kTmXP + 32 * ch, o);
-                tmem_ld_wait();
-                tc_fence_before();
-                mbar_arrive(&s.o_free);
-                const float4 *gm = reinterpret_cast<const float4 *>(M.gbc + 32 * ch);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float4 g4 = gm[q];
-                    o[4 * q] = a.scale * fmaf(g4.x, sq[4 * q], o[4 * q]);
-                    o[4 * q + 1] = a.scale * fmaf(g4.y, sq[4 * q + 1], o[4 * q + 1]);
-                    o[4 * q + 2] = a.scale * fmaf(g4.z, sq[4 * q + 2], o[4 * q + 2]);
-                    o[4 * q + 3] = a.scale * fmaf(g4.w, sq[4 * q + 3], o[4 * q + 3]);
-                }
                 // lanes e and e^1 swap so that each holds two adjacent columns of one row:
                 // even lanes rows 2m, odd lanes rows 2m + 1
                 const int odd = lane & 1;
@@ -1006,8 +1012,17 @@ k_chunk_fused_tc(FusedArgs fa, const __grid_constant__ CUtensorMap tm_q, const _
         __syncthreads();
         uint32_t ld_phase = 0, mma_phase = 0;
         const int units = nch * a.hv;
-        const int stride = (int(gridDim.x) - fa.n_state) * kEngines;
-        for (int u = (int(blockIdx.x) - fa.n_state) * kEngines + e; u < units && !s.abort; u += stride)
+        const int nprep = int(gridDim.x) - fa.n_state;
+        // engine e of prepare CTA i takes units k * 3 * nprep + e * nprep + i:
+        // the first chunks go to engine 0 of every CTA, which starts at once;
+        // engines 1 and 2 start 3 and 6 us later, so that the engines sharing
+        // an SM stay out of step and their load waits overlap the others' work
+        if (e > 0) {
+            const uint64_t t0 = globaltimer_ns();
+            while (globaltimer_ns() - t0 < uint64_t(e) * 3000ull) {
+            }
+        }
+        for (int u = e * nprep + (int(blockIdx.x) - fa.n_state); u < units && !s.abort; u += kEngines * nprep)
             prep_unit(a, w, &tm_q, &tm_k, &tm_v, s, tmem + 128 * e, 1 + e, ld_phase, mma_phase, u / a.hv, u % a.hv);
     }
     tc_fence_before();
