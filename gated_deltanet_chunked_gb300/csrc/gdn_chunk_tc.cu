@@ -112,6 +112,14 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// One arrival per warp: the warp barrier orders every lane's earlier accesses
+// (and, after tcgen05.fence::before_thread_sync, its tensor-memory stores)
+// before lane 0's arrive. Cuts the arrivals on one barrier word 32-fold.
+__device__ __forceinline__ void warp_arrive(uint64_t *bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // inclusive prefix sum of 64 values held two per lane (lane l: 2l, 2l+1)
 __device__ __forceinline__ void warp_scan64(float &a0, float &a1, int lane) {
     a1 += a0;
@@ -574,7 +582,7 @@ __device__ __forceinline__ void prep_unit(const PrefillArgs &a, const TcWs &w, c
 // into the prepared Q and P tiles).
 constexpr int kMathThreads = 256;   // 8 warps: lane quarter (warp % 4) x column half (warp / 4),
                                     // then a copy warp (one polling thread) and an MMA warp
-constexpr int kCopyWarp = 8, kMmaWarp = 9;
+constexpr int kCopyWarpB = 8, kMmaWarp = 9, kCopyWarpM = 10;
 
 // tensor-memory columns (512 allocated)
 constexpr uint32_t kTmSig = 0;    // Sigma accumulator f32 [e][k], 128 columns
@@ -631,10 +639,10 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
             mbar_init(&s.fullB[b], 1);
             mbar_init(&s.emptyB[b], 1);
             mbar_init(&s.fullM[b], 1);
-            mbar_init(&s.emptyM[b], kMathThreads);
+            mbar_init(&s.emptyM[b], kMathThreads / 32);
         }
-        mbar_init(&s.ready_s, kMathThreads);
-        mbar_init(&s.ready_x, kMathThreads);
+        mbar_init(&s.ready_s, kMathThreads / 32);
+        mbar_init(&s.ready_x, kMathThreads / 32);
         mbar_init(&s.mma, 1);
         mbar_init(&s.mma_o, 1);
         fence_mbar_init();
@@ -643,89 +651,74 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
     __syncthreads();
     tc_fence_after();
 
-    if (warp == kCopyWarp) {
-        // --------------------------- copy thread ----------------------------
-        // one thread runs both rings, polling: the epilogue data of a step is
-        // released later than its MMA operands and must not hold back the
-        // next operand loads (two spinning lanes of one warp would starve
-        // each other)
+    if (warp == kCopyWarpB || warp == kCopyWarpM) {
+        // ------------------------- copy threads ----------------------------
+        // one thread per ring, in warps of their own: the epilogue data of a
+        // step is released later than its MMA operands and must not hold back
+        // the next operand loads. Both wait in blocking (suspending) waits.
+        const bool opnd = warp == kCopyWarpB;
         if (lane == 0 && nc > 0) {
-            prefetch_tensormap(tm_k);
-            int cb = -1, cm = -1;  // next step whose operands / epilogue data are loaded
+            if (opnd) prefetch_tensormap(tm_k);
+            uint64_t *full = opnd ? s.fullB : s.fullM, *empty = opnd ? s.emptyB : s.emptyM;
             // chunks 0 .. known of this walk are written by the prepare engines
             // (their flags acquired, so their stores are visible to the copies)
             int known = -1;
-            auto units_ready = [&](int upto) {  // chunks 0 .. upto of this walk
+            auto units_ready = [&](int upto) {  // bounded wait for chunks 0 .. upto of this walk
+                const uint64_t t0 = globaltimer_ns();
                 while (known < upto) {
-                    if (!ld_acquire_gpu(w.ready + size_t(si.first_chunk + known + 1) * a.hv + h)) return false;
-                    ++known;
-                    fence_proxy_async_global();  // the bulk copies read what the flag published
+                    if (ld_acquire_gpu(w.ready + size_t(si.first_chunk + known + 1) * a.hv + h)) {
+                        ++known;
+                        fence_proxy_async_global();  // the bulk copies read what the flag published
+                    } else if (globaltimer_ns() - t0 > 2000000000ull) {
+                        return false;
+                    } else {
+                        __nanosleep(256);
+                    }
                 }
                 return true;
             };
-            uint64_t t0 = globaltimer_ns();
-            while ((cb < nc || cm < nc) && !s.abort) {
-                bool progressed = false;
-                if (cb < nc) {
-                    const int c = cb, b = (c + 1) & 1, use = (c + 1) >> 1;
-                    if (units_ready(min(c + 1, nc - 1)) &&
-                        (use == 0 || mbar_try_wait(&s.emptyB[b], (use - 1) & 1))) {
-                        const bool cur = c >= 0, nxt = c + 1 < nc;
-                        BStage &B = s.bs[b];
-                        mbar_arrive_expect_tx(&s.fullB[b], (cur ? 5 * kTile : 0) + (nxt ? 3 * kTile : 0));
-                        if (cur) {
-                            const int start = si.start + kChunk * c;
-                            const uint8_t *uc = w.unit + (size_t(si.first_chunk + c) * a.hv + h) * kUnitBytes;
-                            for (int hf = 0; hf < 2; ++hf) {
-                                tma_load_3d(B.B1 + hf * kTile, tm_k, 64 * hf, hk, start, &s.fullB[b]);
-                                bulk_load(B.B2 + hf * 2 * kTile + kTile, uc + kUnitQ + hf * kTile, kTile, &s.fullB[b]);
-                            }
-                            bulk_load(B.Pc, uc + kUnitP, kTile, &s.fullB[b]);
-                        }
-                        if (nxt) {
-                            const uint8_t *un = w.unit + (size_t(si.first_chunk + c + 1) * a.hv + h) * kUnitBytes;
-                            for (int hf = 0; hf < 2; ++hf)
-                                bulk_load(B.B2 + hf * 2 * kTile, un + kUnitW + hf * kTile, kTile, &s.fullB[b]);
-                            bulk_load(B.B1 + 2 * kTile, un + kUnitG, kTile, &s.fullB[b]);
-                        }
-                        ++cb;
-                        progressed = true;
-                    }
-                }
-                if (cm < nc) {
-                    const int c = cm, b = (c + 1) & 1, use = (c + 1) >> 1;
-                    if (units_ready(min(c + 1, nc - 1)) &&
-                        (use == 0 || mbar_try_wait(&s.emptyM[b], (use - 1) & 1))) {
-                        const bool nxt = c + 1 < nc;
-                        MStage &M = s.ms[b];
-                        mbar_arrive_expect_tx(&s.fullM[b], nxt ? 2 * kTile + 512 : 0);
-                        if (nxt) {
-                            const size_t un = size_t(si.first_chunk + c + 1) * a.hv + h;
-                            bulk_load(M.Ut, w.unit + un * kUnitBytes + kUnitU, 2 * kTile, &s.fullM[b]);
-                            bulk_load(M.gbn, w.gb + un * 128, 512, &s.fullM[b]);
-                        }
-                        ++cm;
-                        progressed = true;
-                    }
-                }
-                if (progressed) {
-                    t0 = globaltimer_ns();
-                } else if (globaltimer_ns() - t0 > 2000000000ull) {  // no slot freed for 2 s
+            int last = -1;  // last step whose copies were issued
+            for (int c = -1; c < nc && !s.abort; ++c) {
+                const int b = (c + 1) & 1, use = (c + 1) >> 1;
+                const bool cur = c >= 0, nxt = c + 1 < nc;
+                if (!units_ready(min(c + 1, nc - 1)) || (use > 0 && !mbar_wait(&empty[b], (use - 1) & 1))) {
                     s.abort = 1;
+                    break;
                 }
+                if (opnd) {
+                    BStage &B = s.bs[b];
+                    mbar_arrive_expect_tx(&full[b], (cur ? 5 * kTile : 0) + (nxt ? 3 * kTile : 0));
+                    if (cur) {
+                        const int start = si.start + kChunk * c;
+                        const uint8_t *uc = w.unit + (size_t(si.first_chunk + c) * a.hv + h) * kUnitBytes;
+                        for (int hf = 0; hf < 2; ++hf) {
+                            tma_load_3d(B.B1 + hf * kTile, tm_k, 64 * hf, hk, start, &full[b]);
+                            bulk_load(B.B2 + hf * 2 * kTile + kTile, uc + kUnitQ + hf * kTile, kTile, &full[b]);
+                        }
+                        bulk_load(B.Pc, uc + kUnitP, kTile, &full[b]);
+                    }
+                    if (nxt) {
+                        const uint8_t *un = w.unit + (size_t(si.first_chunk + c + 1) * a.hv + h) * kUnitBytes;
+                        for (int hf = 0; hf < 2; ++hf)
+                            bulk_load(B.B2 + hf * 2 * kTile, un + kUnitW + hf * kTile, kTile, &full[b]);
+                        bulk_load(B.B1 + 2 * kTile, un + kUnitG, kTile, &full[b]);
+                    }
+                } else {
+                    MStage &M = s.ms[b];
+                    mbar_arrive_expect_tx(&full[b], nxt ? 2 * kTile + 512 : 0);
+                    if (nxt) {
+                        const size_t un = size_t(si.first_chunk + c + 1) * a.hv + h;
+                        bulk_load(M.Ut, w.unit + un * kUnitBytes + kUnitU, 2 * kTile, &full[b]);
+                        bulk_load(M.gbn, w.gb + un * 128, 512, &full[b]);
+                    }
+                }
+                last = c;
             }
             if (s.abort) {  // bounded drain of copies that may be in flight
-                // last use of stage b among the steps -1 .. next-1 a ring has issued (-1: none)
-                auto last_use = [](int next, int b) {
-                    int c = next - 1;
-                    if (((c + 1) & 1) != b) --c;
-                    return c >= -1 ? (c + 1) >> 1 : -1;
-                };
-                for (int b = 0; b < 2; ++b) {
-                    const int ub = last_use(cb, b), um = last_use(cm, b);
-                    if (ub >= 0) mbar_wait(&s.fullB[b], ub & 1, 100000000ull);
-                    if (um >= 0) mbar_wait(&s.fullM[b], um & 1, 100000000ull);
-                }
+                // the last two steps issued (one per stage); with none issued this
+                // waits out its 0.1 s bound on a phase that never completes
+                for (int c = last; c >= -1 && c >= last - 1; --c)
+                    mbar_wait(&full[(c + 1) & 1], ((c + 1) >> 1) & 1, 100000000ull);
             }
         }
     } else if (warp == kMmaWarp) {
@@ -742,7 +735,7 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
             const uint64_t dstage = uint64_t(sizeof(BStage) >> 4);
             for (int c = -1; c < nc && !s.abort; ++c) {
                 const int b = (c + 1) & 1, use = (c + 1) >> 1;
-                if (!mbar_wait(&s.ready_s, (c + 1) & 1) || !mbar_wait(&s.fullB[b], use & 1)) {
+                if (!mbar_wait_spin(&s.ready_s, (c + 1) & 1) || !mbar_wait_spin(&s.fullB[b], use & 1)) {
                     s.abort = 1;
                     break;
                 }
@@ -752,7 +745,7 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
                 for (int t = 0; t < 8; ++t)  // (c) Sigma_c [-gamma_c W_{c+1} ; Q_c]^T
                     mma_bf16_ts(tmem + kTmV, tmem + kTmSA + 8 * t,
                                 dB2 + ob + (((t >> 2) * 2 * kTile + (t & 3) * 32) >> 4), id_c, t > 0);
-                if (!mbar_wait(&s.ready_x, (c + 1) & 1)) {
+                if (!mbar_wait_spin(&s.ready_x, (c + 1) & 1)) {
                     s.abort = 1;
                     break;
                 }
@@ -807,8 +800,8 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
                 tmem_st16(tmem + lrow + kTmXdA + 16 * ch, r);
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&s.ready_s);
-                mbar_arrive(&s.ready_x);
+                warp_arrive(&s.ready_s);
+                warp_arrive(&s.ready_x);
             }
         }
         // every branch below is warp-uniform (the tcgen05 loads and stores
@@ -816,7 +809,7 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
         // across the warp before they steer control flow
         for (int c = -1; nc > 0 && c < nc && !__any_sync(0xffffffffu, s.abort); ++c) {
             const int b = (c + 1) & 1, use = (c + 1) >> 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(&s.mma, (c + 1) & 1) && mbar_wait(&s.fullM[b], use & 1))) {
+            if (!__all_sync(0xffffffffu, mbar_wait_spin(&s.fullM[b], use & 1) && mbar_wait_spin(&s.mma, (c + 1) & 1))) {
                 s.abort = 1;
                 break;
             }
@@ -825,7 +818,7 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
             // O_c (from the output columns, complete once (b) is) is read
             // before the next step's (c) may overwrite those columns
             auto read_o = [&](float *o) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&s.mma_o, c & 1))) return false;
+                if (!__all_sync(0xffffffffu, mbar_wait_spin(&s.mma_o, c & 1))) return false;
                 tc_fence_after();
                 tmem_ld32(tmem + lrow + kTmO + 32 * ch, o);
                 tmem_ld_wait();
@@ -857,7 +850,7 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
                 if (c >= 0) ok = read_o(o);
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&s.ready_s);
+                warp_arrive(&s.ready_s);
                 // phase 2 (overlaps the next (c)): X_{c+1} = U^T_{c+1} + partial and
                 // X' = X diag(d_{c+1})
 #pragma unroll
@@ -880,7 +873,7 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
                 tmem_st16(tmem + lrow + kTmXdA + 16 * ch, r);
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&s.ready_x);
+                warp_arrive(&s.ready_x);
             } else {
                 float v[64];
                 tmem_ld32(tmem + lrow + kTmSig + 64 * ch, v);
@@ -934,7 +927,7 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
                             *reinterpret_cast<uint32_t *>(obase + size_t(2 * m) * orow) = pr[m];
                 }
             }
-            mbar_arrive(&s.emptyM[b]);
+            warp_arrive(&s.emptyM[b]);
         }
         if (lane == 0) bulk_wait_group_all();  // output stores complete before the CTA exits
     }
