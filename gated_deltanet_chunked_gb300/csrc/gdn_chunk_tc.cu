@@ -892,14 +892,18 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
             }
             if (c >= 0) {
                 // O_c rows r = 32 ch + j, column e
-                // lanes e and e^1 swap so that each holds two adjacent columns of one row:
-                // even lanes rows 2m, odd lanes rows 2m + 1
+                // a 2x2 transpose between lanes e and e^1 on packed pairs: each lane
+                // packs rows 2m, 2m+1 of its column, swaps the word with its
+                // neighbour, and one byte permute leaves even lanes with row 2m and
+                // odd lanes with row 2m+1, in both columns e & ~1 and (e & ~1) + 1
                 const int odd = lane & 1;
+                const uint32_t sel = odd ? 0x3276u : 0x5410u;
                 uint32_t pr[16];
 #pragma unroll
                 for (int m = 0; m < 16; ++m) {
-                    const float other = __shfl_xor_sync(0xffffffffu, odd ? o[2 * m] : o[2 * m + 1], 1);
-                    pr[m] = odd ? pack_bf16x2(other, o[2 * m + 1]) : pack_bf16x2(o[2 * m], other);
+                    const uint32_t pk = pack_bf16x2(o[2 * m], o[2 * m + 1]);
+                    const uint32_t pt = __shfl_xor_sync(0xffffffffu, pk, 1);
+                    pr[m] = __byte_perm(pk, pt, sel);
                 }
                 const int lc = c == nc - 1 ? last_len : kChunk;
                 const int row0 = si.start + kChunk * c + 32 * ch;  // token of the block's first row
