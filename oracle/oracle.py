@@ -14,6 +14,10 @@ Two independent routines (both from the "Lab3 GDN Prefill" page):
   * ``chunked``  -- the chunk form with any chunk size C (section
     "计算过程描述"), including the tail chunk of length l_c = min(C, L - cC).
 
+On top of them, in float64 numpy, the decode front-end (gates from the
+projections, q/k L2 norm, optional bf16 rounding of beta) feeding the
+one-token step; see the block above ``softplus``.
+
 Layouts accepted: packed ``[T_total, H, d]`` with ``cu_seqlens`` (int [N+1]),
 or dense ``[B, T, H, d]`` with ``cu_seqlens=None``. Outputs come back in the
 layout of the inputs, as float64 numpy arrays.
@@ -174,3 +178,89 @@ def recurrent_step(q, k, v, g, beta, scale, state, state_indices=None):
     out[live] = o
     st[idx[live]] = fin
     return out, st
+
+
+# ---------------------------------------------------------------------------
+# Decode front-end: gates from the projections and the q/k L2 norm.
+#
+# Written out in float64 numpy from two pages:
+#  * "sgl-qwen3-5-moe" page, decode node 7
+#    (gdn_packed_recurrent_qk_norm_gating_state_update), steps one and two:
+#      k_bar = k / sqrt(sum_j k_j^2 + 1e-6)
+#      q_bar = (1 / sqrt(d_k)) * q / sqrt(sum_j q_j^2 + 1e-6)
+#      g     = -exp(A_log) * softplus(a + dt_bias),  alpha = exp(g)
+#      beta  = sigmoid(b)
+#    and steps three and four, the gated delta rule, which ``recurrent_step``
+#    already computes.
+#  * "Kestrel_VLLM-24" page, gating row of its CPU-versus-kernel table and the
+#    k_gdn_beta_g kernel it prints: softplus is linear above 20 and exp below
+#    -20; in_proj_b feeds beta and in_proj_a feeds the gate; q and k are
+#    normalised per k-head (q also scaled) before the v-heads are expanded.
+# The page's bf16 rounding of beta belongs to the packed SGLang kernel's
+# precision, not to the method; it is the ``beta_bf16`` option below.
+# ---------------------------------------------------------------------------
+
+SOFTPLUS_THRESHOLD = 20.0
+QK_NORM_EPS = 1e-6
+
+
+def softplus(x):
+    """softplus(x) = log(1 + e^x) with the two overflow branches: x above 20
+    returns x, x below -20 returns e^x (both within e^-20 of the exact value)."""
+    x = np.asarray(x, dtype=np.float64)
+    mid = np.clip(x, -SOFTPLUS_THRESHOLD, SOFTPLUS_THRESHOLD)
+    return np.where(x > SOFTPLUS_THRESHOLD, x,
+                    np.where(x < -SOFTPLUS_THRESHOLD, np.exp(np.minimum(x, 0.0)), np.log1p(np.exp(mid))))
+
+
+def decode_gates(a, b, A_log, dt_bias):
+    """Per-token log-decay g and write strength beta from the gate projections.
+
+    a, b: [N, Hv]; A_log, dt_bias: [Hv]. Returns (g, beta), both [N, Hv]:
+    g = -exp(A_log) * softplus(a + dt_bias) (the decay in the log domain, so
+    alpha = exp(g) is in (0, 1]) and beta = 1 / (1 + exp(-b)).
+    """
+    a, b, A_log, dt_bias = (_f64(x) for x in (a, b, A_log, dt_bias))
+    g = -np.exp(A_log)[None, :] * softplus(a + dt_bias[None, :])
+    with np.errstate(over="ignore"):
+        beta = 1.0 / (1.0 + np.exp(-b))
+    return g, beta
+
+
+def l2_normalise(x, eps=QK_NORM_EPS):
+    """x / sqrt(sum of squares over the last axis + eps): a sum, not a mean."""
+    x = _f64(x)
+    return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
+
+
+def recurrent_step_gated(q, k, v, a, b, A_log, dt_bias, scale, state, state_indices=None,
+                         beta_bf16=False):
+    """One decode step from raw projections, in the order of decode node 7.
+
+    q, k: [N, Hq, dk] raw (not normalised); v: [N, Hv, dv]; a, b: [N, Hv];
+    A_log, dt_bias: [Hv]; ``scale`` is the query scale (1/sqrt(d_k) on the
+    pages), applied once, to q_bar. With ``beta_bf16`` the write strength is
+    rounded to the nearest bf16 (ties to even) before use. Everything else as
+    ``recurrent_step``; returns (o, new_state).
+    """
+    k_bar = l2_normalise(k)
+    q_bar = float(scale) * l2_normalise(q)
+    g, beta = decode_gates(a, b, A_log, dt_bias)
+    if beta_bf16:
+        beta = round_to_bf16(beta)
+    return recurrent_step(q_bar, k_bar, v, g, beta, 1.0, state, state_indices)
+
+
+def round_to_bf16(x):
+    """Nearest bfloat16 value (ties to even) of float64 ``x``, as float64.
+
+    bfloat16 keeps 8 significant bits: x = m * 2^e with 2^7 <= |m| < 2^8 is
+    rounded to an integer m by numpy's round-half-to-even. Below the smallest
+    normal (2^-126) the quantum stays 2^-133 (subnormals)."""
+    x = np.asarray(x, dtype=np.float64)
+    out = np.zeros_like(x)
+    nz = (x != 0) & np.isfinite(x)
+    e = np.maximum(np.floor(np.log2(np.abs(x[nz]))) - 7, -133.0)
+    out[nz] = np.round(x[nz] / np.exp2(e)) * np.exp2(e)
+    out[~nz] = x[~nz]
+    return out

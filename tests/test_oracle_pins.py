@@ -8,7 +8,13 @@ against something the pages or plain mathematics fix:
   * exact equality of the recurrent and chunk forms for several chunk sizes
     (the chunk form with C = 1 is the recurrence; C = L the parallel form),
   * split/resume, GVA head replication and sequence permutation invariants,
-  * planted mistakes: an oracle with a dropped term or a wrong order fails.
+  * planted mistakes: an oracle with a dropped term or a wrong order fails,
+  * the decode front-end: softplus and sigmoid at points with known values,
+    the +-20 softplus branches against the exact function, alpha = 2^-c,
+    the q/k norm as a sum of squares with eps inside the root, single-token
+    closed forms, per-row length invariance, reduction to the plain step
+    through independently inverted gates, and bf16 rounding against the
+    library cast.
 """
 import json
 import math
@@ -269,3 +275,152 @@ def test_hand_example_catches_planted_mistakes(mode):
     o, S = _mutant_recurrent(np.array(i["q"]), np.array(i["k"]), np.array(i["v"]), i["alpha"], i["beta"], mode)
     bad = not (np.allclose(o, ex["expected"]["o"]) and np.allclose(S, ex["expected"]["final_state"]))
     assert bad
+
+
+# --------------------------------------------------------------------------
+# decode front-end (gates from the projections, q/k L2 norm): closed forms
+# --------------------------------------------------------------------------
+def test_softplus_closed_forms_and_branches():
+    sp = oracle.softplus
+    # interior: log(1 + e^x) at points where it is a known number
+    np.testing.assert_allclose(sp(0.0), math.log(2.0), rtol=1e-15)
+    np.testing.assert_allclose(sp(math.log(math.e - 1.0)), 1.0, rtol=1e-14)
+    np.testing.assert_allclose(sp(math.log(math.exp(2.0) - 1.0)), 2.0, rtol=1e-14)
+    x = np.linspace(-19.5, 19.5, 79)
+    np.testing.assert_allclose(sp(x) - sp(-x), x, rtol=0, atol=1e-12)  # softplus(x) - softplus(-x) = x
+    # the branches: identity above 20, e^x below -20, exactly
+    assert sp(25.0) == 25.0 and sp(20.5) == 20.5
+    assert sp(-25.0) == math.exp(-25.0) and sp(-20.5) == math.exp(-20.5)
+    # and each branch is within e^-20 (relative) of the exact function
+    for edge in (20.0, -20.0):
+        xs = edge + np.linspace(-0.2, 0.2, 41)
+        exact = np.logaddexp(0.0, xs)
+        assert np.max(np.abs(sp(xs) - exact) / exact) < 2.1e-9
+
+
+def test_decode_gates_closed_form():
+    c = np.array([1.0, 2.0, 3.0, 0.5])
+    A_log = np.log(c)
+    # a + dt_bias = 0: softplus = ln 2, so g = -c ln 2 and alpha = 2^-c
+    a = np.array([[1.3, -0.7, 0.0, 2.0]])
+    dt_bias = -a[0]
+    b = np.array([[0.0, math.log(3.0), -math.log(3.0), 40.0]])
+    g, beta = oracle.decode_gates(a, b, A_log, dt_bias)
+    np.testing.assert_allclose(np.exp(g), 2.0 ** -c[None], rtol=1e-14)
+    np.testing.assert_allclose(beta, [[0.5, 0.75, 0.25, 1.0 / (1.0 + math.exp(-40.0))]], rtol=1e-15)
+    # linear branch: a + dt_bias = 30 gives g = -30 c exactly
+    g2, _ = oracle.decode_gates(np.full((1, 4), 31.0), b, A_log, np.full(4, -1.0))
+    np.testing.assert_allclose(g2, -30.0 * c[None], rtol=1e-15)
+    # sigmoid saturates without overflow warnings for large negative b
+    _, b3 = oracle.decode_gates(a, np.full((1, 4), -800.0), A_log, dt_bias)
+    assert np.all(b3 == 0.0)
+
+
+def test_l2_normalise_is_sum_of_squares_with_eps_inside():
+    x = np.zeros((2, 1, 128))
+    x[0, 0, 0], x[0, 0, 1] = 3.0, 4.0
+    y = oracle.l2_normalise(x)
+    np.testing.assert_allclose(y[0, 0, :2], np.array([3.0, 4.0]) / math.sqrt(25.0 + 1e-6), rtol=1e-15)
+    assert np.all(y[0, 0, 2:] == 0.0) and np.all(y[1] == 0.0)  # a zero row stays zero
+
+
+def _gate_inputs_for(alpha_c, beta_b, hv):
+    """a, b, A_log, dt_bias with alpha = 2^-alpha_c and beta = sigmoid(beta_b)."""
+    A_log = np.log(np.full(hv, float(alpha_c)))
+    return np.zeros((1, hv)), np.full((1, hv), float(beta_b)), A_log, np.zeros(hv)
+
+
+@pytest.mark.parametrize("scale", [1.0 / math.sqrt(128.0), 0.37])
+def test_gated_step_single_token_closed_form(scale):
+    """S0 = 0, one token, q and k along e_0 with raw lengths 2 and 5:
+    o = (q_bar . k_bar) beta v with q_bar . k_bar = scale * 2 * 5 / (sqrt(4 + eps) sqrt(25 + eps)),
+    and the new state is k_bar^T (beta v): row 0 only."""
+    dk = dv = 128
+    hq, hv = 1, 2
+    q = np.zeros((1, hq, dk)); q[0, 0, 0] = 2.0
+    k = np.zeros((1, hq, dk)); k[0, 0, 0] = 5.0
+    v = np.random.default_rng(3).standard_normal((1, hv, dv))
+    a, _, A_log, dt_bias = _gate_inputs_for(1.0, 0.0, hv)
+    b = np.array([[0.0, math.log(3.0)]])
+    beta = np.array([0.5, 0.75])
+    o, S = oracle.recurrent_step_gated(q, k, v, a, b, A_log, dt_bias, scale, np.zeros((1, hv, dk, dv)))
+    qk = scale * 10.0 / (math.sqrt(4.0 + 1e-6) * math.sqrt(25.0 + 1e-6))
+    np.testing.assert_allclose(o[0], qk * beta[:, None] * v[0], rtol=1e-13)
+    np.testing.assert_allclose(S[0, :, 0, :], (5.0 / math.sqrt(25.0 + 1e-6)) * beta[:, None] * v[0], rtol=1e-13)
+    assert np.all(S[0, :, 1:, :] == 0.0)
+
+
+def test_gated_step_zero_key_only_decays():
+    """k = 0 writes nothing: S' = 2^-c S0 and o = 2^-c q_bar S0 with q = 3 e_j."""
+    dk = dv = 128
+    hv, c, j, scale = 2, 3.0, 17, 0.25
+    rng = np.random.default_rng(4)
+    S0 = rng.standard_normal((1, hv, dk, dv))
+    q = np.zeros((1, 1, dk)); q[0, 0, j] = 3.0
+    a, b, A_log, dt_bias = _gate_inputs_for(c, 0.3, hv)
+    o, S = oracle.recurrent_step_gated(q, np.zeros((1, 1, dk)), rng.standard_normal((1, hv, dv)),
+                                       a, b, A_log, dt_bias, scale, S0)
+    np.testing.assert_allclose(S, 2.0 ** -c * S0, rtol=1e-14)
+    np.testing.assert_allclose(o[0], 2.0 ** -c * scale * 3.0 / math.sqrt(9.0 + 1e-6) * S0[0, :, j, :],
+                               rtol=1e-13)
+
+
+def test_gated_step_invariant_to_per_head_qk_lengths():
+    """Normalisation is per (token, k-head) over d_k: rescaling each raw q/k
+    row by its own factor (lengths far above sqrt(eps)) changes nothing."""
+    rng = np.random.default_rng(5)
+    N, hq, hv, dk, dv = 3, 2, 4, 16, 8
+    q, k = rng.standard_normal((N, hq, dk)), rng.standard_normal((N, hq, dk))
+    v = rng.standard_normal((N, hv, dv))
+    a, b = rng.standard_normal((N, hv)), rng.standard_normal((N, hv))
+    A_log, dt_bias = rng.uniform(0, 2, hv), rng.uniform(-4, 0, hv)
+    S0 = rng.standard_normal((N, hv, dk, dv))
+    o1, S1 = oracle.recurrent_step_gated(q, k, v, a, b, A_log, dt_bias, 0.3, S0)
+    fq, fk = rng.uniform(1, 50, (N, hq, 1)), rng.uniform(1, 50, (N, hq, 1))
+    o2, S2 = oracle.recurrent_step_gated(q * fq, k * fk, v, a, b, A_log, dt_bias, 0.3, S0)
+    assert rel(o2, o1) < 1e-7 and rel(S2, S1) < 1e-7
+
+
+def test_gated_step_reduces_to_plain_step():
+    """Gates inverted independently (softplus^-1 through expm1, sigmoid^-1 as
+    the logit) and keys of length 1000 (eps negligible) give back the plain
+    decode step on the pre-normalised inputs."""
+    rng = np.random.default_rng(6)
+    N, hq, hv, dk, dv = 4, 2, 4, 32, 16
+    q, k, v, g, beta, _, _ = rand_inputs(7, [N], hq, hv, dk, dv, s0=False)
+    S0 = rng.standard_normal((N, hv, dk, dv))
+    A_log = rng.uniform(-1, 2, hv)
+    dt_bias = rng.uniform(-5, 1, hv)
+    sp = -g / np.exp(A_log)[None]  # the softplus value each gate needs
+    a = np.log(np.expm1(sp)) - dt_bias[None]
+    b = np.log(beta / (1 - beta))
+    o1, S1 = oracle.recurrent_step_gated(1000 * q, 1000 * k, v, a, b, A_log, dt_bias, 0.125, S0, [2, 0, 3, 1])
+    o2, S2 = oracle.recurrent_step(q, k, v, g, beta, 0.125, S0, [2, 0, 3, 1])
+    assert rel(o1, o2) < 1e-10 and rel(S1, S2) < 1e-10
+
+
+def test_round_to_bf16_matches_library_cast():
+    import torch
+
+    rng = np.random.default_rng(8)
+    x = np.concatenate([rng.uniform(0, 1, 4000), 10.0 ** rng.uniform(-45, 0, 2000),
+                        # exact ties between two bf16 neighbours, both parities
+                        (np.arange(256, 512) + 0.5) / 512.0, -rng.uniform(0, 3, 100), [0.0, 1.0]])
+    lib = torch.tensor(x, dtype=torch.float64).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(oracle.round_to_bf16(x), lib)
+
+
+def test_gated_step_beta_bf16_option():
+    rng = np.random.default_rng(9)
+    N, hq, hv, dk, dv = 2, 1, 2, 16, 8
+    q, k = rng.standard_normal((N, hq, dk)), rng.standard_normal((N, hq, dk))
+    v, a, b = rng.standard_normal((N, hv, dv)), rng.standard_normal((N, hv)), rng.standard_normal((N, hv))
+    A_log, dt_bias, S0 = rng.uniform(0, 1, hv), rng.uniform(-3, 0, hv), rng.standard_normal((N, hv, dk, dv))
+    o1, S1 = oracle.recurrent_step_gated(q, k, v, a, b, A_log, dt_bias, 0.5, S0, beta_bf16=True)
+    g, beta = oracle.decode_gates(a, b, A_log, dt_bias)
+    o2, S2 = oracle.recurrent_step(0.5 * oracle.l2_normalise(q), oracle.l2_normalise(k), v, g,
+                                   oracle.round_to_bf16(beta), 1.0, S0)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(S1, S2)
+    o3, _ = oracle.recurrent_step_gated(q, k, v, a, b, A_log, dt_bias, 0.5, S0)
+    assert rel(o3, o1) > 1e-5  # the rounding is visible
