@@ -9,7 +9,8 @@ state, f32 final state), inputs resident in HBM. Between timed steps the L2 is
 flushed by writing a 512 MiB buffer (the inputs, 104 MB, would fit in the
 126 MB L2). Prints ONE JSON line (rank 0). The decode step (256 sequences x 32
 v-heads, f32 state read and written in place) is measured in the same run and
-reported under "decode".
+reported under "decode"; the same step fed raw q/k and gate projections (the
+front-end computed in the kernel) under "decode_gated".
 
 Multi-GPU (torchrun, one rank per GPU): every rank runs its own replica of the
 workload (weak scaling: the GDN core shards over sequences and heads with no
@@ -354,6 +355,7 @@ def run_ours(args, world, rank, local):
            "serial_ms_per_step": e2e_serial_ms}
 
     decode = None if args.no_decode else run_decode(args, dev, world, peaks, peak_src)
+    decode_gated = None if args.no_decode else run_decode(args, dev, world, peaks, peak_src, gated=True)
     clocks.stop()
     clk = clocks.summary(t_start, t_end)
 
@@ -369,7 +371,7 @@ def run_ours(args, world, rank, local):
                    "chunk": 64, "initial_state": "zero", "final_state": "f32",
                    "l2": "flushed between timed steps (512 MiB write)", "parallelism": f"replicas x{world}"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": gpu_launches,
-        "kernels": kernels, "decode": decode,
+        "kernels": kernels, "decode": decode, "decode_gated": decode_gated,
         "step_ms": {"median": statistics.median(step_ms), "p10": sorted(step_ms)[len(step_ms) // 10],
                     "p90": sorted(step_ms)[(9 * len(step_ms)) // 10]},
     }
@@ -377,20 +379,28 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def run_decode(args, dev, world, peaks, peak_src):
+def run_decode(args, dev, world, peaks, peak_src, gated=False):
+    """Times the decode step; ``gated`` runs gdn_recurrent_step_gated (raw q/k
+    and gate projections in, front-end in the kernel) instead."""
     from gated_deltanet_chunked_gb300 import gdn
 
     w = DECODE
     state = W.make_decode_state(w).to(dev)
+    make = W.make_decode_step_gated if gated else W.make_decode_step
     sets = []
     for s in range(4):
-        inp = W.make_decode_step(w, s)
+        inp = make(w, s)
         sets.append({k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()})
     out = torch.empty_like(sets[0]["v"])
+    A_log, dt_bias = (t.to(dev) for t in W.make_decode_gate_params(w))
 
     def step(i):
         x = sets[i % len(sets)]
-        gdn.gdn_recurrent_step(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], state, out=out)
+        if gated:
+            gdn.gdn_recurrent_step_gated(x["q"], x["k"], x["v"], x["a"], x["b"], A_log, dt_bias, x["scale"],
+                                         state, out=out)
+        else:
+            gdn.gdn_recurrent_step(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], state, out=out)
 
     for i in range(max(3, args.warmup)):
         step(i)
@@ -412,16 +422,20 @@ def run_decode(args, dev, world, peaks, peak_src):
     ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(e0, e1)) / steps, world, dev)
     n_pairs = w.num_seqs * w.hv
     state_bytes = 2 * n_pairs * 128 * 128 * 4
-    io_bytes = w.num_seqs * (w.hq * 128 * 2 * 2 + w.hv * 128 * 2 * 2 + w.hv * 8)
+    # q, k, v, out in bf16; g, beta (or a, b) f32 per (sequence, v-head); A_log, dt_bias f32 per v-head
+    io_bytes = w.num_seqs * (w.hq * 128 * 2 * 2 + w.hv * 128 * 2 * 2 + w.hv * 8) + (w.hv * 8 if gated else 0)
     total = state_bytes + io_bytes
-    n, kms, nt = prof.get("recurrent_step", (0, 0.0, 0))
+    kname = "recurrent_step_gated" if gated else "recurrent_step"
+    n, kms, nt = prof.get(kname, (0, 0.0, 0))
     k_ms = kms / max(nt, 1)
     return {
         "workload": w.name, "steps": steps, "ms_per_step": ms, "value": world * total / (ms * 1e-3) / 1e9,
         "unit": "GB/s", "state_bytes_per_step": state_bytes, "bytes_per_step": total,
-        "roofline": {"kernel": "recurrent_step", "bound": "hbm", "achieved": total / (k_ms * 1e-3) / 1e9,
+        "inputs": ("raw q/k, gate projections a/b, A_log/dt_bias (front-end in the kernel)" if gated
+                   else "normalised q/k, g, beta"),
+        "roofline": {"kernel": kname, "bound": "hbm", "achieved": total / (k_ms * 1e-3) / 1e9,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": total / (k_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "traffic": ncu_traffic("recurrent_step"),
+                     "frac": total / (k_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "traffic": ncu_traffic(kname),
                      "peak_source": f"{peak_src} (hbm_gbs, burst copy)"},
         "l2": "state (537 MB) larger than L2; no flush",
     }

@@ -32,6 +32,7 @@ int *status_ptr() {
 }
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Checks shared by prefill and decode. Returns GDN_OK or the error code.
@@ -87,7 +88,7 @@ using namespace gdn;
 
 extern "C" {
 
-int gdn_version(void) { return 101; }
+int gdn_version(void) { return 102; }
 
 const char *gdn_status_string(int status) {
     switch (status) {
@@ -169,8 +170,30 @@ int gdn_recurrent_step(const gdn_problem *p, const void *q, const void *k, const
     if (int64_t(p->num_seqs) * p->hv >= (int64_t(1) << 31)) return GDN_EINVAL;
     int *status = status_ptr();
     if (!status) return GDN_ECUDA;
-    return cuda_status(launch_recurrent_step(*p, q, k, v, g, beta, scale, state, state_indices, out, status,
-                                             static_cast<cudaStream_t>(stream)));
+    return cuda_status(launch_recurrent_step(*p, q, k, v, g, beta, nullptr, scale, state, state_indices, out,
+                                             status, static_cast<cudaStream_t>(stream)));
+}
+
+int gdn_recurrent_step_gated(const gdn_problem *p, const void *q, const void *k, const void *v, const float *a,
+                             const float *b, const float *A_log, const float *dt_bias, float scale, float *state,
+                             const int32_t *state_indices, void *out, void *stream) {
+    int st = check_common(p);
+    if (st) return st;
+    if (p->total_tokens != p->num_seqs) return GDN_EINVAL;
+    if (p->num_state_slots < 0 || (!state_indices && p->num_state_slots < p->num_seqs)) return GDN_EINVAL;
+    if (p->num_seqs > 0) {
+        if (!q || !k || !v || !a || !b || !A_log || !dt_bias || !out || !state) return GDN_EINVAL;
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(state) ||
+            (state_indices && !aligned16(state_indices)))
+            return GDN_EINVAL;
+        if (!aligned4(a) || !aligned4(b) || !aligned4(A_log) || !aligned4(dt_bias)) return GDN_EINVAL;
+    }
+    if (int64_t(p->num_seqs) * p->hv >= (int64_t(1) << 31)) return GDN_EINVAL;
+    int *status = status_ptr();
+    if (!status) return GDN_ECUDA;
+    const DecodeFront front{a, b, A_log, dt_bias};
+    return cuda_status(launch_recurrent_step(*p, q, k, v, nullptr, nullptr, &front, scale, state, state_indices,
+                                             out, status, static_cast<cudaStream_t>(stream)));
 }
 
 int gdn_read_device_status(void *stream, int clear) {

@@ -90,8 +90,17 @@ size_t prefill_simt_workspace(int max_chunks, int hv);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, void *ws_data, cudaStream_t s);
 int *prefill_tc_ready_flags(void *ws_data, int max_chunks, int hv);
 size_t prefill_tc_workspace(int max_chunks, int hv);
+// Raw inputs of the decode front-end (gdn_recurrent_step_gated): gate
+// projections a, b [num_seqs, hv] and per-head A_log, dt_bias [hv].
+struct DecodeFront {
+    const float *a, *b, *A_log, *dt_bias;
+};
+// `front` null: g and beta are given and q, k are used as they are.
+// `front` set: g and beta are null and computed from it, q and k are
+// L2-normalised in the kernel.
 cudaError_t launch_recurrent_step(const gdn_problem &p, const void *q, const void *k, const void *v,
-                                  const float *g, const float *beta, float scale, float *state,
-                                  const int32_t *state_indices, void *out, int *status, cudaStream_t s);
+                                  const float *g, const float *beta, const DecodeFront *front, float scale,
+                                  float *state, const int32_t *state_indices, void *out, int *status,
+                                  cudaStream_t s);
 
 }  // namespace gdn

@@ -20,6 +20,17 @@
 //   o   = scale (alpha r + qk d)     (= scale q (alpha S_old + k^T d) exactly)
 //   S'  = alpha S_old + k^T d
 // so the new state never has to be re-read to produce the output.
+//
+// The gated variant (gdn_recurrent_step_gated) adds the front-end of decode
+// node 7 on the sgl-qwen3-5-moe page, steps one and two, with the softplus
+// branches of the Kestrel_VLLM-24 page's gating kernel:
+//   k_bar = k / sqrt(|k|^2 + 1e-6),  q_bar = scale * q / sqrt(|q|^2 + 1e-6)
+//   g = -exp(A_log) softplus(a + dt_bias),  alpha = exp(g),  beta = sigmoid(b)
+// The norms are taken over the raw rows already in shared memory; instead of
+// rescaling the rows, rk = 1/|k| and rq = 1/|q| fold into the scalars:
+//   d' = rk beta (v - alpha rk p),  S' = alpha S_old + k^T d',
+//   o  = scale rq (alpha r + qk d')
+// with p, r, qk the raw-row reductions above. The state traffic is unchanged.
 #include "gdn_common.cuh"
 
 namespace gdn {
@@ -33,15 +44,37 @@ __device__ __forceinline__ float ldx(const void *p, size_t i) {
     return to_f32<T>(static_cast<const T *>(p)[i]);
 }
 
+// four consecutive elements starting at a multiple of 4 (one 8- or 16-byte load)
 template <typename T>
+__device__ __forceinline__ float4 ld4(const void *p, size_t i);
+template <>
+__device__ __forceinline__ float4 ld4<float>(const void *p, size_t i) {
+    return *reinterpret_cast<const float4 *>(static_cast<const float *>(p) + i);
+}
+template <>
+__device__ __forceinline__ float4 ld4<__nv_bfloat16>(const void *p, size_t i) {
+    const uint2 u = *reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(p) + i);
+    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.x));
+    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u.y));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+
+// log(1 + e^x), linear above 20 and e^x below -20 (no overflow of e^x)
+__device__ __forceinline__ float softplus_f(float x) {
+    if (x > 20.f) return x;
+    if (x < -20.f) return expf(x);
+    return log1pf(expf(x));
+}
+
+template <typename T, bool kFront>
 __global__ void __launch_bounds__(kRThreads, 2)
 k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const void *__restrict__ v,
-                 const float *__restrict__ g, const float *__restrict__ beta, float scale,
+                 const float *__restrict__ g, const float *__restrict__ beta, DecodeFront front, float scale,
                  float *__restrict__ state, const int32_t *__restrict__ idx, void *__restrict__ out,
                  int num_seqs, int hq, int hv, int slots, int *status) {
     __shared__ float ks[kHeadDim], qs[kHeadDim];
     __shared__ float4 red_p[kRThreads / 32][32], red_r[kRThreads / 32][32];
-    __shared__ float qk_s;
+    __shared__ float qk_s, rk_s, rq_s;
     const int pair = blockIdx.x;
     const int n = pair / hv, h = pair % hv, hk = h / (hv / hq);
     const int tid = threadIdx.x, lane = tid & 31, wrow = tid >> 5;
@@ -52,21 +85,55 @@ k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const v
         return;
     }
     float4 *S = reinterpret_cast<float4 *>(state + (size_t(slot) * hv + h) * kHeadDim * kHeadDim);
-    // issue all state loads first: 16 independent 128-bit loads per thread
+    // The small inputs are issued first so that the gate arithmetic and the
+    // q/k staging overlap the 64 KiB state read instead of following it.
+    const size_t nh = size_t(n) * hv + h;
+    const size_t vo = nh * kHeadDim + 4 * lane;
+    float ga, gb, gA = 0.f, gdt = 0.f;
+    if (kFront) {
+        ga = front.a[nh];
+        gb = front.b[nh];
+        gA = front.A_log[h];
+        gdt = front.dt_bias[h];
+    } else {
+        ga = g[nh];
+        gb = beta[nh];
+    }
+    const float4 vv = ld4<T>(v, vo);
+    float kq_k = 0.f, kq_q = 0.f;
+    if (tid < kHeadDim) {
+        const size_t qk_off = (size_t(n) * hq + hk) * kHeadDim + tid;
+        kq_k = ldx<T>(k, qk_off);
+        kq_q = ldx<T>(q, qk_off);
+    }
+    // all state loads: 16 independent 128-bit loads per thread
     float4 s[kRowsPerThread];
 #pragma unroll
     for (int i = 0; i < kRowsPerThread; ++i) s[i] = S[(wrow + 8 * i) * 32 + lane];
+    float alpha, b;
+    if (kFront) {
+        alpha = expf(-expf(gA) * softplus_f(ga + gdt));
+        b = 1.f / (1.f + expf(-gb));
+    } else {
+        alpha = expf(ga);
+        b = gb;
+    }
     if (tid < kHeadDim) {
-        const size_t qk_off = (size_t(n) * hq + hk) * kHeadDim + tid;
-        ks[tid] = ldx<T>(k, qk_off);
-        qs[tid] = ldx<T>(q, qk_off);
+        ks[tid] = kq_k;
+        qs[tid] = kq_q;
     }
     __syncthreads();
-    if (wrow == 0) {  // q . k by warp 0
+    // q . k by warp 0; for the front-end |k|^2 by warp 1 and |q|^2 by warp 2
+    if (wrow < (kFront ? 3 : 1)) {
+        const float *x = wrow == 2 ? qs : ks, *y = wrow == 0 ? qs : x;
         float acc = 0.f;
-        for (int d = lane; d < kHeadDim; d += 32) acc = fmaf(qs[d], ks[d], acc);
+        for (int d = lane; d < kHeadDim; d += 32) acc = fmaf(x[d], y[d], acc);
         for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) qk_s = acc;
+        if (lane == 0) {
+            if (wrow == 0) qk_s = acc;
+            else if (wrow == 1) rk_s = rsqrtf(acc + 1e-6f);
+            else rq_s = rsqrtf(acc + 1e-6f);
+        }
     }
     float4 p = make_float4(0.f, 0.f, 0.f, 0.f), r = p;
 #pragma unroll
@@ -88,21 +155,24 @@ k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const v
         p.x += a.x; p.y += a.y; p.z += a.z; p.w += a.w;
         r.x += b.x; r.y += b.y; r.z += b.z; r.w += b.w;
     }
-    const float alpha = expf(g[size_t(n) * hv + h]);
-    const float b = beta[size_t(n) * hv + h];
-    const size_t vo = (size_t(n) * hv + h) * kHeadDim + 4 * lane;
+    float rk = 1.f, oscale = scale;
+    if (kFront) {
+        rk = rk_s;
+        oscale = scale * rq_s;
+    }
+    const float ak = alpha * rk, bk = b * rk;  // d' = rk beta (v - alpha rk p)
     float4 d;
-    d.x = b * (ldx<T>(v, vo + 0) - alpha * p.x);
-    d.y = b * (ldx<T>(v, vo + 1) - alpha * p.y);
-    d.z = b * (ldx<T>(v, vo + 2) - alpha * p.z);
-    d.w = b * (ldx<T>(v, vo + 3) - alpha * p.w);
+    d.x = bk * (vv.x - ak * p.x);
+    d.y = bk * (vv.y - ak * p.y);
+    d.z = bk * (vv.z - ak * p.z);
+    d.w = bk * (vv.w - ak * p.w);
     if (wrow == 0) {
         const float qk = qk_s;
         T *o = static_cast<T *>(out) + vo;
-        o[0] = from_f32<T>(scale * fmaf(alpha, r.x, qk * d.x));
-        o[1] = from_f32<T>(scale * fmaf(alpha, r.y, qk * d.y));
-        o[2] = from_f32<T>(scale * fmaf(alpha, r.z, qk * d.z));
-        o[3] = from_f32<T>(scale * fmaf(alpha, r.w, qk * d.w));
+        o[0] = from_f32<T>(oscale * fmaf(alpha, r.x, qk * d.x));
+        o[1] = from_f32<T>(oscale * fmaf(alpha, r.y, qk * d.y));
+        o[2] = from_f32<T>(oscale * fmaf(alpha, r.z, qk * d.z));
+        o[3] = from_f32<T>(oscale * fmaf(alpha, r.w, qk * d.w));
     }
 #pragma unroll
     for (int i = 0; i < kRowsPerThread; ++i) {
@@ -119,18 +189,18 @@ k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const v
 }  // namespace
 
 cudaError_t launch_recurrent_step(const gdn_problem &p, const void *q, const void *k, const void *v,
-                                  const float *g, const float *beta, float scale, float *state,
-                                  const int32_t *state_indices, void *out, int *status, cudaStream_t s) {
+                                  const float *g, const float *beta, const DecodeFront *front, float scale,
+                                  float *state, const int32_t *state_indices, void *out, int *status,
+                                  cudaStream_t s) {
     const unsigned pairs = unsigned(p.num_seqs) * unsigned(p.hv);
     if (pairs == 0) return cudaSuccess;
-    LaunchScope scope(GDN_K_RECURRENT_STEP, s);
-    if (p.io_dtype == GDN_DT_BF16)
-        k_recurrent_step<__nv_bfloat16><<<pairs, kRThreads, 0, s>>>(q, k, v, g, beta, scale, state, state_indices,
-                                                                   out, p.num_seqs, p.hq, p.hv,
-                                                                   p.num_state_slots, status);
-    else
-        k_recurrent_step<float><<<pairs, kRThreads, 0, s>>>(q, k, v, g, beta, scale, state, state_indices, out,
-                                                           p.num_seqs, p.hq, p.hv, p.num_state_slots, status);
+    LaunchScope scope(front ? GDN_K_RECURRENT_STEP_GATED : GDN_K_RECURRENT_STEP, s);
+    const DecodeFront f = front ? *front : DecodeFront{nullptr, nullptr, nullptr, nullptr};
+    auto kern = p.io_dtype == GDN_DT_BF16
+                    ? (front ? k_recurrent_step<__nv_bfloat16, true> : k_recurrent_step<__nv_bfloat16, false>)
+                    : (front ? k_recurrent_step<float, true> : k_recurrent_step<float, false>);
+    kern<<<pairs, kRThreads, 0, s>>>(q, k, v, g, beta, f, scale, state, state_indices, out, p.num_seqs, p.hq,
+                                    p.hv, p.num_state_slots, status);
     return cudaGetLastError();
 }
 

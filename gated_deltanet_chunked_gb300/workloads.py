@@ -13,6 +13,9 @@ Recipe (numpy PCG64, seed = 1000 + workload index):
   beta  = sigmoid(N(0, 1))         (float32)
   S0    ~ N(0, sigma_s^2)          (float32, sigma_s = 0.1 or 0.05)
 Varlen lengths are drawn from the same generator, uniform in [100, 8000].
+Decode front-end inputs (raw projections, nothing normalised):
+  q, k  ~ N(0, 1), cast          a, b ~ N(0, 1) (float32, [N, Hv])
+  A_log = log U[1, 16]           dt_bias ~ U[-6.9, -2.25]   (float32, [Hv])
 """
 from __future__ import annotations
 
@@ -150,3 +153,24 @@ def make_custom_prefill(seed, lengths, hq, hv, io_dtype=torch.float32, s0_sigma=
         s0 = torch.from_numpy(_normal(rng, (N, hv, dk, dv), sigma=s0_sigma))
     return dict(q=q, k=k, v=v, g=g, beta=beta, initial_state=s0, cu_seqlens=torch.from_numpy(cu),
                 scale=1.0 / math.sqrt(dk), num_seqs=N, total_tokens=T)
+
+
+def make_decode_gate_params(w: Workload, seed: Optional[int] = None):
+    """Per-v-head parameters of the decode front-end: A_log, dt_bias [Hv] f32."""
+    rng = np.random.Generator(np.random.PCG64([w.seed if seed is None else seed, 0]))
+    A_log = np.log(rng.uniform(1.0, 16.0, size=w.hv)).astype(np.float32)
+    dt_bias = rng.uniform(-6.9, -2.25, size=w.hv).astype(np.float32)
+    return torch.from_numpy(A_log), torch.from_numpy(dt_bias)
+
+
+def make_decode_step_gated(w: Workload, step: int, a_sigma: float = 1.0):
+    """Raw inputs of gated decode step ``step``: q, k [N, Hq, 128] and v
+    [N, Hv, 128] in the io dtype, gate projections a, b [N, Hv] f32."""
+    rng = np.random.Generator(np.random.PCG64([w.seed, 1 + step, 1]))
+    N = w.num_seqs
+    q = torch.from_numpy(_normal(rng, (N, w.hq, DK))).to(w.io_dtype)
+    k = torch.from_numpy(_normal(rng, (N, w.hq, DK))).to(w.io_dtype)
+    v = torch.from_numpy(_normal(rng, (N, w.hv, DV))).to(w.io_dtype)
+    a = torch.from_numpy(_normal(rng, (N, w.hv), sigma=a_sigma))
+    b = torch.from_numpy(_normal(rng, (N, w.hv)))
+    return dict(q=q, k=k, v=v, a=a, b=b, scale=1.0 / math.sqrt(DK))

@@ -18,7 +18,14 @@
  *            GVA head map h_qk = floor(h_v / (Hv / Hq)).
  *  [SGL]   "sgl-qwen3-5-moe" (rainlin-net), decode node 7
  *          (gdn_packed_recurrent_qk_norm_gating_state_update): one token,
- *          decay -> predict -> correct -> read, state held in f32.
+ *          decay -> predict -> correct -> read, state held in f32; its
+ *          steps one and two: q/k L2 norm with eps 1e-6 inside the root and
+ *          the query scale, gates g = -exp(A_log) softplus(a + dt_bias),
+ *          beta = sigmoid(b).
+ *  [Kestrel] "Kestrel_VLLM-24 · GDN 线性注意力上 GPU" (wsisp.com), its
+ *          CPU-versus-kernel table: softplus with linear / exponential
+ *          branches beyond +-20, q/k normalised per k-head before the
+ *          v-heads are expanded.
  *
  * Conventions shared by every entry point
  *  - All tensor pointers are DEVICE pointers owned by the caller. The library
@@ -29,7 +36,8 @@
  *      v, out [total_tokens, hv, dv]      io_dtype
  *      g, beta[total_tokens, hv]          float32 (g is the raw log-decay)
  *      state  [num_seqs or slots, hv, dk, dv] float32
- *    Every pointer must be 16-byte aligned.
+ *    Every pointer must be 16-byte aligned (the per-head gate inputs of
+ *    gdn_recurrent_step_gated only 4-byte aligned).
  *  - Supported: dk = dv = 128, chunk size 64 (fixed), hv % hq == 0,
  *    io_dtype GDN_DT_F32 (SIMT f32 arithmetic) or GDN_DT_BF16 (tensor-core
  *    bf16 operands with f32 accumulation and f32 state). Anything else returns
@@ -161,6 +169,36 @@ int gdn_recurrent_step(const gdn_problem *p, const void *q, const void *k, const
                        float *state, const int32_t *state_indices,
                        void *out, void *stream);
 
+/* Decode step from the raw projections: gdn_recurrent_step with its
+ * front-end fused in (decode node 7 of [SGL], steps one and two; the gating
+ * kernel of [Kestrel]). For each sequence n and v-head h (k-head
+ * kh = h / (hv / hq)):
+ *   k_bar = k[n,kh] / sqrt(sum_j k[n,kh,j]^2 + 1e-6)
+ *   q_bar = scale * q[n,kh] / sqrt(sum_j q[n,kh,j]^2 + 1e-6)
+ *   g     = -exp(A_log[h]) * softplus(a[n,h] + dt_bias[h]),  alpha = exp(g)
+ *   beta  = 1 / (1 + exp(-b[n,h]))
+ * where softplus(x) is x above 20, exp(x) below -20, log1p(exp(x)) between.
+ * Then, as gdn_recurrent_step with scale 1 on q_bar:
+ *   S = alpha * state[s,h];  d = beta (v[n,h] - k_bar S);
+ *   state[s,h] = S + k_bar^T d;  out[n,h] = q_bar state[s,h].
+ *   q, k      [num_seqs, hq, 128] raw (not normalised), io dtype
+ *   v, out    [num_seqs, hv, 128], io dtype
+ *   a, b      [num_seqs, hv] f32: the gate projections (a drives the decay,
+ *             b the write strength)
+ *   A_log, dt_bias [hv] f32: per-head parameters
+ *   scale     the query scale, 1/sqrt(128) on the pages; applied once
+ *   state, state_indices: as gdn_recurrent_step (f32, in place; negative
+ *             index = padding slot, skipped; index >= num_state_slots is
+ *             skipped and recorded as GDN_EDEVICE_INPUT).
+ * All pointers are caller-owned device memory; q, k, v, out, state and
+ * state_indices 16-byte aligned, a, b, A_log, dt_bias 4-byte aligned.
+ * Returns GDN_EINVAL (nothing launched) on a bad descriptor or pointer.
+ * beta is used in f32, without the bf16 rounding of [SGL]'s packed kernel. */
+int gdn_recurrent_step_gated(const gdn_problem *p, const void *q, const void *k, const void *v,
+                             const float *a, const float *b, const float *A_log, const float *dt_bias,
+                             float scale, float *state, const int32_t *state_indices,
+                             void *out, void *stream);
+
 /* Synchronises `stream`, returns the device status word (GDN_OK or the first
  * device-side error recorded since the last clear) and clears it when
  * `clear` is non-zero. Returns GDN_ECUDA if the CUDA calls themselves fail. */
@@ -182,7 +220,8 @@ typedef enum gdn_kernel {
     GDN_K_OUTPUT_SIMT = 3,        /* f32: chunk output */
     GDN_K_RECURRENT_STEP = 4,     /* decode step */
     GDN_K_CHUNK_FUSED_TC = 5,     /* bf16: chunk preparation and state walk, one co-resident grid (tensor cores) */
-    GDN_K_COUNT = 6
+    GDN_K_RECURRENT_STEP_GATED = 6, /* decode step with the gate / q-k norm front-end */
+    GDN_K_COUNT = 7
 } gdn_kernel;
 
 /* Turns per-kernel CUDA-event timing on (non-zero) or off for every later

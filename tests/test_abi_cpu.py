@@ -109,3 +109,23 @@ def test_recurrent_step_rejects_bad_problems():
     assert step(problem(**{**ok, "dk": 96})) == gdn.GDN_EUNSUPPORTED
     assert step(problem(**ok), ptr=FAKE + 2) == gdn.GDN_EINVAL
     assert step(problem(**ok), idx=FAKE + 4) == gdn.GDN_EINVAL
+
+
+def test_recurrent_step_gated_rejects_bad_problems():
+    lib = gdn.load()
+    P = ctypes.c_void_p
+
+    def step(p, idx=None, ptr=FAKE, gate=FAKE, b=FAKE):
+        return lib.gdn_recurrent_step_gated(ctypes.byref(p), P(ptr), P(ptr), P(ptr), P(gate), P(b), P(gate),
+                                            P(gate), ctypes.c_float(1.0), P(ptr), None if idx is None else P(idx),
+                                            P(ptr), None)
+
+    ok = dict(batch=4, seqlen=1, num_seqs=4, total_tokens=4, num_state_slots=4)
+    assert step(problem(**{**ok, "num_state_slots": 3})) == gdn.GDN_EINVAL
+    assert step(problem(**{**ok, "total_tokens": 5})) == gdn.GDN_EINVAL
+    assert step(problem(**{**ok, "dv": 64})) == gdn.GDN_EUNSUPPORTED
+    assert step(problem(**{**ok, "flags": 2})) == gdn.GDN_EUNSUPPORTED
+    assert step(problem(**ok), ptr=FAKE + 4) == gdn.GDN_EINVAL  # tensors want 16-byte alignment
+    assert step(problem(**ok), gate=FAKE + 2) == gdn.GDN_EINVAL  # gate inputs want 4-byte alignment
+    assert step(problem(**ok), b=0) == gdn.GDN_EINVAL
+    assert step(problem(**ok), idx=FAKE + 4) == gdn.GDN_EINVAL
