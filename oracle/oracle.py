@@ -264,3 +264,27 @@ def round_to_bf16(x):
     out[nz] = np.round(x[nz] / np.exp2(e)) * np.exp2(e)
     out[~nz] = x[~nz]
     return out
+
+
+# ---------------------------------------------------------------------------
+# Output gate: head-wise RMSNorm of the read-out, then the SiLU gate of z
+# ("sgl-qwen3-5-moe" page, node output_rmsnorm_silu_gate; "Kestrel_VLLM-24"
+# page, the gated-RMSNorm row: rsqrt scale, then the weight, then silu(z)).
+#   y = (o / sqrt(mean_j o_j^2 + eps)) * weight * silu(z),  over one head's d_v
+# The norm comes before the gate (norm_before_gate); the weight multiplies
+# directly (no 1 + w parameterisation). The page leaves eps as a symbol; the
+# callers pass it.
+# ---------------------------------------------------------------------------
+
+def silu(x):
+    """x * sigmoid(x) = x / (1 + e^-x)."""
+    x = _f64(x)
+    with np.errstate(over="ignore"):
+        return x / (1.0 + np.exp(-x))
+
+
+def gated_rmsnorm(o, z, weight, eps):
+    """o, z: [..., d_v]; weight: [d_v]. Returns y of o's shape in float64."""
+    o, z, weight = _f64(o), _f64(z), _f64(weight)
+    rms = np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + float(eps))
+    return (o / rms) * weight * silu(z)

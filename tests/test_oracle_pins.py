@@ -14,7 +14,10 @@ against something the pages or plain mathematics fix:
     the q/k norm as a sum of squares with eps inside the root, single-token
     closed forms, per-row length invariance, reduction to the plain step
     through independently inverted gates, and bf16 rounding against the
-    library cast.
+    library cast,
+  * the output gate: silu at points with known values, the RMS of a constant
+    row and of a one-hot row (a mean, not a sum), norm before gate, per-head
+    normalisation.
 """
 import json
 import math
@@ -424,3 +427,54 @@ def test_gated_step_beta_bf16_option():
     np.testing.assert_array_equal(S1, S2)
     o3, _ = oracle.recurrent_step_gated(q, k, v, a, b, A_log, dt_bias, 0.5, S0)
     assert rel(o3, o1) > 1e-5  # the rounding is visible
+
+
+# --------------------------------------------------------------------------
+# output gate: head-wise RMSNorm, then SiLU(z)
+# --------------------------------------------------------------------------
+def test_silu_closed_forms():
+    s = oracle.silu
+    assert s(0.0)[0] == 0.0
+    np.testing.assert_allclose(s(math.log(3.0)), 0.75 * math.log(3.0), rtol=1e-15)
+    np.testing.assert_allclose(s(-math.log(3.0)), -0.25 * math.log(3.0), rtol=1e-15)
+    x = np.linspace(-30, 30, 121)
+    np.testing.assert_allclose(s(x) - s(-x), x, rtol=0, atol=1e-13)  # silu(x) - silu(-x) = x
+    assert s(-800.0)[0] == 0.0 and s(800.0)[0] == 800.0
+
+
+def test_gated_rmsnorm_constant_row():
+    """o = c 1: the RMS is sqrt(c^2 + eps), so y = c / sqrt(c^2 + eps) w silu(z)."""
+    rng = np.random.default_rng(11)
+    d = 128
+    w, z = rng.uniform(0.5, 2, d), rng.standard_normal((1, d))
+    for c, eps in ((3.0, 1e-6), (-0.01, 1e-5), (2.0, 0.0)):
+        y = oracle.gated_rmsnorm(np.full((1, d), c), z, w, eps)
+        np.testing.assert_allclose(y, c / math.sqrt(c * c + eps) * w * oracle.silu(z), rtol=1e-14)
+
+
+def test_gated_rmsnorm_mean_not_sum():
+    """A single non-zero channel a: mean of squares a^2 / d, so y_0 = sqrt(d) w_0 silu(z_0) for eps = 0."""
+    d = 128
+    o = np.zeros((2, d)); o[0, 0] = 5.0; o[1, 7] = -0.25
+    z = np.full((2, d), 1.5)
+    w = np.linspace(0.5, 1.5, d)
+    y = oracle.gated_rmsnorm(o, z, w, 0.0)
+    g = 1.5 / (1.0 + math.exp(-1.5))
+    np.testing.assert_allclose(y[0, 0], math.sqrt(d) * w[0] * g, rtol=1e-14)
+    np.testing.assert_allclose(y[1, 7], -math.sqrt(d) * w[7] * g, rtol=1e-14)
+    assert np.count_nonzero(y) == 2
+
+
+def test_gated_rmsnorm_norm_before_gate_and_per_head():
+    """The gate does not enter the RMS (y / silu(z) does not depend on z), and
+    each head row is normalised on its own (rescaling one head leaves the
+    others and, for eps = 0, itself unchanged)."""
+    rng = np.random.default_rng(12)
+    o = rng.standard_normal((3, 4, 128))
+    w = rng.uniform(0.5, 2, 128)
+    z1, z2 = rng.uniform(0.5, 3, o.shape), rng.uniform(-3, -0.5, o.shape)
+    y1, y2 = oracle.gated_rmsnorm(o, z1, w, 1e-6), oracle.gated_rmsnorm(o, z2, w, 1e-6)
+    np.testing.assert_allclose(y1 / oracle.silu(z1), y2 / oracle.silu(z2), rtol=1e-12)
+    f = rng.uniform(0.1, 10, (3, 4, 1))
+    np.testing.assert_allclose(oracle.gated_rmsnorm(o * f, z1, w, 0.0), oracle.gated_rmsnorm(o, z1, w, 0.0),
+                               rtol=1e-12)
