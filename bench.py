@@ -10,7 +10,9 @@ flushed by writing a 512 MiB buffer (the inputs, 104 MB, would fit in the
 126 MB L2). Prints ONE JSON line (rank 0). The decode step (256 sequences x 32
 v-heads, f32 state read and written in place) is measured in the same run and
 reported under "decode"; the same step fed raw q/k and gate projections (the
-front-end computed in the kernel) under "decode_gated".
+front-end and the output gate computed in the kernel) under "decode_gated";
+the stand-alone output gate (gdn_gated_rmsnorm) over the prefill's
+[4096, 32, 128] read-out under "output_gate".
 
 Multi-GPU (torchrun, one rank per GPU): every rank runs its own replica of the
 workload (weak scaling: the GDN core shards over sequences and heads with no
@@ -46,6 +48,20 @@ PREFILL = W.WORKLOADS["prefill_T4096_hq16_hv32"]
 DECODE = W.WORKLOADS["decode_N256_hq16_hv32"]
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 512 << 20
+L2_NOTE = "flushed between timed launches (512 MiB write)"
+
+
+class L2Flush:
+    """Evicts the L2 between timed launches by writing a buffer four times its
+    size. (Measured on the prefill step: as fast as no flush at all, since
+    the step's own 240 MB of traffic evicts its inputs anyway; the dirty
+    lines the write leaves cost it nothing measurable.)"""
+
+    def __init__(self, dev):
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def __call__(self):
+        self.w.fill_(1)
 
 
 # --------------------------------------------------------------------------
@@ -234,14 +250,14 @@ def run_ours(args, world, rank, local):
     prob = gdn.prefill_problem(d["q"], d["v"], N, packed=True)
     ws = torch.empty(gdn.gdn_chunk_fwd_workspace_size(prob), dtype=torch.uint8, device=dev)
     cu = torch.tensor([0, T], dtype=torch.int32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     def step():
         gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], initial_state=None, cu_seqlens=cu,
                           out=out, final_state=fin, workspace=ws)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     assert gdn.gdn_read_device_status() == gdn.GDN_OK
@@ -256,7 +272,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     t_start = time.time()
     for i in range(args.steps):
-        flush.zero_()
+        flush()
         ev0[i].record()
         step()
         ev1[i].record()
@@ -356,6 +372,7 @@ def run_ours(args, world, rank, local):
 
     decode = None if args.no_decode else run_decode(args, dev, world, peaks, peak_src)
     decode_gated = None if args.no_decode else run_decode(args, dev, world, peaks, peak_src, gated=True)
+    output_gate = None if args.no_decode else run_gate_norm(args, dev, world, peaks, peak_src)
     clocks.stop()
     clk = clocks.summary(t_start, t_end)
 
@@ -369,9 +386,9 @@ def run_ours(args, world, rank, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "B": 1, "T": T, "hq": w.hq, "hv": w.hv, "dk": 128, "dv": 128,
                    "chunk": 64, "initial_state": "zero", "final_state": "f32",
-                   "l2": "flushed between timed steps (512 MiB write)", "parallelism": f"replicas x{world}"},
+                   "l2": L2_NOTE, "parallelism": f"replicas x{world}"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": gpu_launches,
-        "kernels": kernels, "decode": decode, "decode_gated": decode_gated,
+        "kernels": kernels, "decode": decode, "decode_gated": decode_gated, "output_gate": output_gate,
         "step_ms": {"median": statistics.median(step_ms), "p10": sorted(step_ms)[len(step_ms) // 10],
                     "p90": sorted(step_ms)[(9 * len(step_ms)) // 10]},
     }
@@ -393,12 +410,13 @@ def run_decode(args, dev, world, peaks, peak_src, gated=False):
         sets.append({k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()})
     out = torch.empty_like(sets[0]["v"])
     A_log, dt_bias = (t.to(dev) for t in W.make_decode_gate_params(w))
+    z, norm_w = (t.to(dev) for t in W.make_output_gate(w.seed, w.num_seqs, w.hv, w.io_dtype))
 
     def step(i):
         x = sets[i % len(sets)]
         if gated:
             gdn.gdn_recurrent_step_gated(x["q"], x["k"], x["v"], x["a"], x["b"], A_log, dt_bias, x["scale"],
-                                         state, out=out)
+                                         state, out=out, z=z, norm_weight=norm_w, norm_eps=1e-6)
         else:
             gdn.gdn_recurrent_step(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], state, out=out)
 
@@ -423,7 +441,10 @@ def run_decode(args, dev, world, peaks, peak_src, gated=False):
     n_pairs = w.num_seqs * w.hv
     state_bytes = 2 * n_pairs * 128 * 128 * 4
     # q, k, v, out in bf16; g, beta (or a, b) f32 per (sequence, v-head); A_log, dt_bias f32 per v-head
-    io_bytes = w.num_seqs * (w.hq * 128 * 2 * 2 + w.hv * 128 * 2 * 2 + w.hv * 8) + (w.hv * 8 if gated else 0)
+    # gated: + z (bf16, like v) per (sequence, v-head) and the 128-float norm weight
+    io_bytes = w.num_seqs * (w.hq * 128 * 2 * 2 + w.hv * 128 * 2 * 2 + w.hv * 8)
+    if gated:
+        io_bytes += w.hv * 8 + w.num_seqs * w.hv * 128 * 2 + 128 * 4
     total = state_bytes + io_bytes
     kname = "recurrent_step_gated" if gated else "recurrent_step"
     n, kms, nt = prof.get(kname, (0, 0.0, 0))
@@ -431,13 +452,56 @@ def run_decode(args, dev, world, peaks, peak_src, gated=False):
     return {
         "workload": w.name, "steps": steps, "ms_per_step": ms, "value": world * total / (ms * 1e-3) / 1e9,
         "unit": "GB/s", "state_bytes_per_step": state_bytes, "bytes_per_step": total,
-        "inputs": ("raw q/k, gate projections a/b, A_log/dt_bias (front-end in the kernel)" if gated
-                   else "normalised q/k, g, beta"),
+        "inputs": ("raw q/k, gate projections a/b, A_log/dt_bias, output gate z + RMSNorm weight "
+                   "(front-end and output gate in the kernel)" if gated else "normalised q/k, g, beta"),
         "roofline": {"kernel": kname, "bound": "hbm", "achieved": total / (k_ms * 1e-3) / 1e9,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": total / (k_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "traffic": ncu_traffic(kname),
                      "peak_source": f"{peak_src} (hbm_gbs, burst copy)"},
         "l2": "state (537 MB) larger than L2; no flush",
+    }
+
+
+def run_gate_norm(args, dev, world, peaks, peak_src):
+    """Times gdn_gated_rmsnorm over the prefill workload's read-out tensor
+    [4096, 32, 128] bf16 (o, z in; y out). Launches rotate over four sets of
+    (o, z, y), 403 MB in all, so each launch finds its inputs evicted from L2
+    by the three launches before it (a write flush would instead leave 126 MB
+    of dirty lines whose write-back this streaming kernel would pay for)."""
+    from gated_deltanet_chunked_gb300 import gdn
+
+    w = PREFILL
+    sets = []
+    for i in range(4):
+        z, weight, o = (t.to(dev) for t in W.make_output_gate(w.seed + 97 * i, w.seqlen, w.hv, w.io_dtype,
+                                                                with_o=True))
+        sets.append((o, z, weight, torch.empty_like(o)))
+    for i in range(max(3, args.warmup)):
+        o, z, weight, y = sets[i % 4]
+        gdn.gdn_gated_rmsnorm(o, z, weight, 1e-6, out=y)
+    steps = max(12, min(args.steps, 100))
+    gdn.gdn_profile_collect(reset=True)
+    gdn.gdn_profile_enable(True)
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        o, z, weight, y = sets[i % 4]
+        gdn.gdn_gated_rmsnorm(o, z, weight, 1e-6, out=y)
+    torch.cuda.synchronize()
+    barrier(world)
+    gdn.gdn_profile_enable(False)
+    prof = gdn.gdn_profile_collect(reset=True)
+    n, kms, nt = prof.get("gated_rmsnorm", (0, 0.0, 0))
+    k_ms = max_over_ranks(kms / max(nt, 1), world, dev)
+    total = 3 * o.numel() * o.element_size() + 128 * 4
+    return {
+        "workload": f"{w.name} read-out", "rows": w.seqlen * w.hv, "steps": steps, "ms_per_launch": k_ms,
+        "value": world * total / (k_ms * 1e-3) / 1e9, "unit": "GB/s", "bytes_per_launch": total,
+        "roofline": {"kernel": "gated_rmsnorm", "bound": "hbm", "achieved": total / (k_ms * 1e-3) / 1e9,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": total / (k_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                     "traffic": ncu_traffic("gated_rmsnorm"),
+                     "peak_source": f"{peak_src} (hbm_gbs, burst copy)"},
+        "l2": "inputs rotate over 4 sets of o, z, y (403 MB, larger than L2); no flush",
     }
 
 

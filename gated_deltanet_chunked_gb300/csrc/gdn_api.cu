@@ -176,7 +176,8 @@ int gdn_recurrent_step(const gdn_problem *p, const void *q, const void *k, const
 
 int gdn_recurrent_step_gated(const gdn_problem *p, const void *q, const void *k, const void *v, const float *a,
                              const float *b, const float *A_log, const float *dt_bias, float scale, float *state,
-                             const int32_t *state_indices, void *out, void *stream) {
+                             const int32_t *state_indices, const void *z, const float *norm_weight,
+                             float norm_eps, void *out, void *stream) {
     int st = check_common(p);
     if (st) return st;
     if (p->total_tokens != p->num_seqs) return GDN_EINVAL;
@@ -187,13 +188,32 @@ int gdn_recurrent_step_gated(const gdn_problem *p, const void *q, const void *k,
             (state_indices && !aligned16(state_indices)))
             return GDN_EINVAL;
         if (!aligned4(a) || !aligned4(b) || !aligned4(A_log) || !aligned4(dt_bias)) return GDN_EINVAL;
+        if (z && (!norm_weight || !aligned16(z) || !aligned16(norm_weight))) return GDN_EINVAL;
     }
+    if (z && !(norm_eps >= 0.f)) return GDN_EINVAL;
     if (int64_t(p->num_seqs) * p->hv >= (int64_t(1) << 31)) return GDN_EINVAL;
     int *status = status_ptr();
     if (!status) return GDN_ECUDA;
-    const DecodeFront front{a, b, A_log, dt_bias};
+    const DecodeFront front{a, b, A_log, dt_bias, z, z ? norm_weight : nullptr, norm_eps};
     return cuda_status(launch_recurrent_step(*p, q, k, v, nullptr, nullptr, &front, scale, state, state_indices,
                                              out, status, static_cast<cudaStream_t>(stream)));
+}
+
+int gdn_gated_rmsnorm(const gdn_problem *p, const void *o, const void *z, const float *weight, float eps, void *y,
+                      void *stream) {
+    if (!p || p->hv <= 0 || p->total_tokens < 0) return GDN_EINVAL;
+    if (p->io_dtype != GDN_DT_F32 && p->io_dtype != GDN_DT_BF16) return GDN_EINVAL;
+    if (p->dv != kHeadDim) return p->dv > 0 ? GDN_EUNSUPPORTED : GDN_EINVAL;
+    if (!(eps >= 0.f)) return GDN_EINVAL;
+    const long long rows = (long long)p->total_tokens * p->hv;
+    if (rows > 0) {
+        if (!o || !z || !weight || !y) return GDN_EINVAL;
+        if (!aligned16(o) || !aligned16(z) || !aligned16(weight) || !aligned16(y)) return GDN_EINVAL;
+    }
+    int *status = status_ptr();
+    if (!status) return GDN_ECUDA;
+    return cuda_status(launch_gated_rmsnorm(o, z, weight, eps, y, rows, p->io_dtype, status,
+                                            static_cast<cudaStream_t>(stream)));
 }
 
 int gdn_read_device_status(void *stream, int clear) {

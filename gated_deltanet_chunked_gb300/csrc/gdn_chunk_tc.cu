@@ -108,18 +108,6 @@ __device__ __forceinline__ float exp_decay(float x) {
     return y;
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// One arrival per warp: the warp barrier orders every lane's earlier accesses
-// (and, after tcgen05.fence::before_thread_sync, its tensor-memory stores)
-// before lane 0's arrive. Cuts the arrivals on one barrier word 32-fold.
-__device__ __forceinline__ void warp_arrive(uint64_t *bar) {
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-}
-
 // inclusive prefix sum of 64 values held two per lane (lane l: 2l, 2l+1)
 __device__ __forceinline__ void warp_scan64(float &a0, float &a1, int lane) {
     a1 += a0;

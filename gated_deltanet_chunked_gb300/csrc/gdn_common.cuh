@@ -85,16 +85,34 @@ class LaunchScope {
 
 // Host-side launchers implemented in the kernel translation units.
 cudaError_t launch_chunk_table(const PrefillArgs &a, cudaStream_t s);
+cudaError_t launch_gated_rmsnorm(const void *o, const void *z, const float *weight, float eps, void *y,
+                                 long long rows, int io_dtype, int *status, cudaStream_t s);
 cudaError_t launch_prefill_simt(const PrefillArgs &a, void *ws_data, cudaStream_t s);
 size_t prefill_simt_workspace(int max_chunks, int hv);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, void *ws_data, cudaStream_t s);
 int *prefill_tc_ready_flags(void *ws_data, int max_chunks, int hv);
 size_t prefill_tc_workspace(int max_chunks, int hv);
 // Raw inputs of the decode front-end (gdn_recurrent_step_gated): gate
-// projections a, b [num_seqs, hv] and per-head A_log, dt_bias [hv].
+// projections a, b [num_seqs, hv] and per-head A_log, dt_bias [hv]; and the
+// optional output gate: z [num_seqs, hv, 128] (io dtype) with the RMSNorm
+// weight [128] and eps (z null: no output gate).
 struct DecodeFront {
     const float *a, *b, *A_log, *dt_bias;
+    const void *z;
+    const float *norm_weight;
+    float norm_eps;
 };
+
+// x * sigmoid(x) = x / (1 + e^-x), the output gate's activation. e^-x is
+// taken as 2^(-x log2 e) on the base-2 exponential unit and the quotient
+// through the approximate reciprocal (both relative errors ~1e-7): x = -inf
+// side gives x * 0, the +inf side x * 1.
+__device__ __forceinline__ float silu_f(float x) {
+    float e, r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * -1.4426950408889634f));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
+    return x * r;
+}
 // `front` null: g and beta are given and q, k are used as they are.
 // `front` set: g and beta are null and computed from it, q and k are
 // L2-normalised in the kernel.

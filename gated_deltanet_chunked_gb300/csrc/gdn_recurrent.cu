@@ -31,6 +31,10 @@
 //   d' = rk beta (v - alpha rk p),  S' = alpha S_old + k^T d',
 //   o  = scale rq (alpha r + qk d')
 // with p, r, qk the raw-row reductions above. The state traffic is unchanged.
+// With an output gate z (the sgl-qwen3-5-moe page's output_rmsnorm_silu_gate,
+// norm before gate), warp 0, which holds the head's 128 outputs, finishes
+//   y = o / sqrt(mean(o^2) + eps) * weight * silu(z)
+// in f32 before the single rounding to the output dtype.
 #include "gdn_common.cuh"
 
 namespace gdn {
@@ -42,6 +46,20 @@ constexpr int kRowsPerThread = kHeadDim / (kRThreads / 32);  // 16
 template <typename T>
 __device__ __forceinline__ float ldx(const void *p, size_t i) {
     return to_f32<T>(static_cast<const T *>(p)[i]);
+}
+
+// four consecutive elements starting at a multiple of 4 (one 8- or 16-byte store)
+template <typename T>
+__device__ __forceinline__ void st4(void *p, size_t i, const float4 &x);
+template <>
+__device__ __forceinline__ void st4<float>(void *p, size_t i, const float4 &x) {
+    *reinterpret_cast<float4 *>(static_cast<float *>(p) + i) = x;
+}
+template <>
+__device__ __forceinline__ void st4<__nv_bfloat16>(void *p, size_t i, const float4 &x) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y), hi = __floats2bfloat162_rn(x.z, x.w);
+    *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p) + i) =
+        make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
 }
 
 // four consecutive elements starting at a multiple of 4 (one 8- or 16-byte load)
@@ -66,7 +84,7 @@ __device__ __forceinline__ float softplus_f(float x) {
     return log1pf(expf(x));
 }
 
-template <typename T, bool kFront>
+template <typename T, bool kFront, bool kGateOut>
 __global__ void __launch_bounds__(kRThreads, 2)
 k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const void *__restrict__ v,
                  const float *__restrict__ g, const float *__restrict__ beta, DecodeFront front, float scale,
@@ -74,7 +92,8 @@ k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const v
                  int num_seqs, int hq, int hv, int slots, int *status) {
     __shared__ float ks[kHeadDim], qs[kHeadDim];
     __shared__ float4 red_p[kRThreads / 32][32], red_r[kRThreads / 32][32];
-    __shared__ float qk_s, rk_s, rq_s;
+    __shared__ float qk_s, rk_s, rq_s, alpha_s, beta_s;
+    __shared__ float4 gz_s[32];  // weight * silu(z), 4 channels per lane
     const int pair = blockIdx.x;
     const int n = pair / hv, h = pair % hv, hk = h / (hv / hq);
     const int tid = threadIdx.x, lane = tid & 31, wrow = tid >> 5;
@@ -85,21 +104,30 @@ k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const v
         return;
     }
     float4 *S = reinterpret_cast<float4 *>(state + (size_t(slot) * hv + h) * kHeadDim * kHeadDim);
-    // The small inputs are issued first so that the gate arithmetic and the
-    // q/k staging overlap the 64 KiB state read instead of following it.
+    // The small inputs are issued first, each by the warp that uses it, so that
+    // they arrive while the 64 KiB state read is still in flight. Nothing but
+    // the q/k staging stands before the first barrier: the front-end's scalar
+    // work runs in warps that would otherwise wait at the second one.
+    constexpr bool gate_out = kFront && kGateOut;
+    constexpr int kGateWarp = 3, kZWarp = 4;
     const size_t nh = size_t(n) * hv + h;
     const size_t vo = nh * kHeadDim + 4 * lane;
-    float ga, gb, gA = 0.f, gdt = 0.f;
-    if (kFront) {
+    float ga = 0.f, gb = 0.f, gA = 0.f, gdt = 0.f;
+    if (kFront && wrow == kGateWarp) {
         ga = front.a[nh];
         gb = front.b[nh];
         gA = front.A_log[h];
         gdt = front.dt_bias[h];
-    } else {
+    } else if (!kFront) {
         ga = g[nh];
         gb = beta[nh];
     }
     const float4 vv = ld4<T>(v, vo);
+    float4 zz = make_float4(0.f, 0.f, 0.f, 0.f), nw = zz;
+    if (gate_out && wrow == kZWarp) {
+        zz = ld4<T>(front.z, vo);
+        nw = *reinterpret_cast<const float4 *>(front.norm_weight + 4 * lane);
+    }
     float kq_k = 0.f, kq_q = 0.f;
     if (tid < kHeadDim) {
         const size_t qk_off = (size_t(n) * hq + hk) * kHeadDim + tid;
@@ -110,20 +138,13 @@ k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const v
     float4 s[kRowsPerThread];
 #pragma unroll
     for (int i = 0; i < kRowsPerThread; ++i) s[i] = S[(wrow + 8 * i) * 32 + lane];
-    float alpha, b;
-    if (kFront) {
-        alpha = expf(-expf(gA) * softplus_f(ga + gdt));
-        b = 1.f / (1.f + expf(-gb));
-    } else {
-        alpha = expf(ga);
-        b = gb;
-    }
     if (tid < kHeadDim) {
         ks[tid] = kq_k;
         qs[tid] = kq_q;
     }
     __syncthreads();
-    // q . k by warp 0; for the front-end |k|^2 by warp 1 and |q|^2 by warp 2
+    // q . k by warp 0; for the front-end |k|^2 by warp 1 and |q|^2 by warp 2,
+    // the gates by warp 3 and weight * silu(z) by warp 4
     if (wrow < (kFront ? 3 : 1)) {
         const float *x = wrow == 2 ? qs : ks, *y = wrow == 0 ? qs : x;
         float acc = 0.f;
@@ -135,6 +156,12 @@ k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const v
             else rq_s = rsqrtf(acc + 1e-6f);
         }
     }
+    if (kFront && wrow == kGateWarp && lane == 0) {
+        alpha_s = expf(-expf(gA) * softplus_f(ga + gdt));
+        beta_s = 1.f / (1.f + expf(-gb));
+    }
+    if (gate_out && wrow == kZWarp)
+        gz_s[lane] = make_float4(nw.x * silu_f(zz.x), nw.y * silu_f(zz.y), nw.z * silu_f(zz.z), nw.w * silu_f(zz.w));
     float4 p = make_float4(0.f, 0.f, 0.f, 0.f), r = p;
 #pragma unroll
     for (int i = 0; i < kRowsPerThread; ++i) {
@@ -155,6 +182,14 @@ k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const v
         p.x += a.x; p.y += a.y; p.z += a.z; p.w += a.w;
         r.x += b.x; r.y += b.y; r.z += b.z; r.w += b.w;
     }
+    float alpha, b;
+    if (kFront) {
+        alpha = alpha_s;
+        b = beta_s;
+    } else {
+        alpha = expf(ga);
+        b = gb;
+    }
     float rk = 1.f, oscale = scale;
     if (kFront) {
         rk = rk_s;
@@ -166,13 +201,25 @@ k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const v
     d.y = bk * (vv.y - ak * p.y);
     d.z = bk * (vv.z - ak * p.z);
     d.w = bk * (vv.w - ak * p.w);
+    // the read-out (warp 0 holds the head's 128 outputs), then the state
     if (wrow == 0) {
         const float qk = qk_s;
-        T *o = static_cast<T *>(out) + vo;
-        o[0] = from_f32<T>(oscale * fmaf(alpha, r.x, qk * d.x));
-        o[1] = from_f32<T>(oscale * fmaf(alpha, r.y, qk * d.y));
-        o[2] = from_f32<T>(oscale * fmaf(alpha, r.z, qk * d.z));
-        o[3] = from_f32<T>(oscale * fmaf(alpha, r.w, qk * d.w));
+        float4 y;
+        y.x = oscale * fmaf(alpha, r.x, qk * d.x);
+        y.y = oscale * fmaf(alpha, r.y, qk * d.y);
+        y.z = oscale * fmaf(alpha, r.z, qk * d.z);
+        y.w = oscale * fmaf(alpha, r.w, qk * d.w);
+        if (gate_out) {  // y = o / rms(o) * weight * silu(z), the head's 128 values in this warp
+            float ss = y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
+            for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            const float inv = rsqrtf(ss * (1.f / kHeadDim) + front.norm_eps);
+            const float4 gz = gz_s[lane];
+            y.x *= inv * gz.x;
+            y.y *= inv * gz.y;
+            y.z *= inv * gz.z;
+            y.w *= inv * gz.w;
+        }
+        st4<T>(out, vo, y);
     }
 #pragma unroll
     for (int i = 0; i < kRowsPerThread; ++i) {
@@ -195,10 +242,14 @@ cudaError_t launch_recurrent_step(const gdn_problem &p, const void *q, const voi
     const unsigned pairs = unsigned(p.num_seqs) * unsigned(p.hv);
     if (pairs == 0) return cudaSuccess;
     LaunchScope scope(front ? GDN_K_RECURRENT_STEP_GATED : GDN_K_RECURRENT_STEP, s);
-    const DecodeFront f = front ? *front : DecodeFront{nullptr, nullptr, nullptr, nullptr};
+    const DecodeFront f = front ? *front : DecodeFront{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0.f};
+    const bool gate = front && front->z;
     auto kern = p.io_dtype == GDN_DT_BF16
-                    ? (front ? k_recurrent_step<__nv_bfloat16, true> : k_recurrent_step<__nv_bfloat16, false>)
-                    : (front ? k_recurrent_step<float, true> : k_recurrent_step<float, false>);
+                    ? (gate ? k_recurrent_step<__nv_bfloat16, true, true>
+                            : front ? k_recurrent_step<__nv_bfloat16, true, false>
+                                    : k_recurrent_step<__nv_bfloat16, false, false>)
+                    : (gate ? k_recurrent_step<float, true, true>
+                            : front ? k_recurrent_step<float, true, false> : k_recurrent_step<float, false, false>);
     kern<<<pairs, kRThreads, 0, s>>>(q, k, v, g, beta, f, scale, state, state_indices, out, p.num_seqs, p.hq,
                                     p.hv, p.num_state_slots, status);
     return cudaGetLastError();

@@ -49,6 +49,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// One arrival per warp: the warp barrier orders every lane's earlier accesses
+// (and, after tcgen05.fence::before_thread_sync, its tensor-memory stores)
+// before lane 0's arrive. Cuts the arrivals on one barrier word 32-fold.
+__device__ __forceinline__ void warp_arrive(uint64_t *bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // Non-blocking test of a phase (never suspends the thread; for polling loops).
 __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;

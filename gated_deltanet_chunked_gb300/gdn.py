@@ -6,7 +6,7 @@ no fallback: if libgdn.so cannot be built or loaded, ``load()`` raises.
 
 The entry points keep the C names:
   gdn_chunk_fwd, gdn_chunk_fwd_workspace_size, gdn_recurrent_step,
-  gdn_recurrent_step_gated, gdn_read_device_status, gdn_status_string, gdn_version.
+  gdn_recurrent_step_gated, gdn_gated_rmsnorm, gdn_read_device_status, gdn_status_string, gdn_version.
 """
 from __future__ import annotations
 
@@ -24,8 +24,8 @@ GDN_DT_F32, GDN_DT_BF16 = 0, 1
 
 SYMBOLS = ("gdn_chunk_fwd", "gdn_chunk_fwd_workspace_size", "gdn_recurrent_step", "gdn_read_device_status",
            "gdn_status_string", "gdn_version", "gdn_profile_enable", "gdn_profile_collect", "gdn_kernel_name",
-           "gdn_chunk_fwd_noalloc", "gdn_recurrent_step_gated")
-GDN_K_COUNT = 7
+           "gdn_chunk_fwd_noalloc", "gdn_recurrent_step_gated", "gdn_gated_rmsnorm")
+GDN_K_COUNT = 8
 
 
 class GdnProblem(ctypes.Structure):
@@ -61,7 +61,9 @@ def load(path: Optional[str] = None):
             lib.gdn_recurrent_step.argtypes = [P, _vp, _vp, _vp, _fp, _fp, ctypes.c_float, _fp, _ip, _vp, _vp]
             lib.gdn_recurrent_step.restype = ctypes.c_int
             lib.gdn_recurrent_step_gated.argtypes = [P, _vp, _vp, _vp, _fp, _fp, _fp, _fp, ctypes.c_float, _fp,
-                                                     _ip, _vp, _vp]
+                                                     _ip, _vp, _fp, ctypes.c_float, _vp, _vp]
+            lib.gdn_gated_rmsnorm.argtypes = [P, _vp, _vp, _fp, ctypes.c_float, _vp, _vp]
+            lib.gdn_gated_rmsnorm.restype = ctypes.c_int
             lib.gdn_recurrent_step_gated.restype = ctypes.c_int
             lib.gdn_read_device_status.argtypes = [_vp, ctypes.c_int]
             lib.gdn_read_device_status.restype = ctypes.c_int
@@ -190,18 +192,35 @@ def gdn_recurrent_step(q, k, v, g, beta, scale, state, state_indices=None, out=N
 
 
 def gdn_recurrent_step_gated(q, k, v, a, b, A_log, dt_bias, scale, state, state_indices=None, out=None,
-                             stream=None):
+                             stream=None, z=None, norm_weight=None, norm_eps=1e-6):
     """Decode step from raw q/k and the gate projections a, b [N, Hv] with
-    per-head A_log, dt_bias [Hv] (all f32); ``state`` is updated in place."""
+    per-head A_log, dt_bias [Hv] (all f32); ``state`` is updated in place.
+    With ``z`` [N, Hv, 128] and ``norm_weight`` [128] f32 the output gate
+    (head-wise RMSNorm, then silu(z)) is applied before the store."""
     N, hq, dk = q.shape
     prob = GdnProblem(N, 1, N, N, hq, v.shape[1], dk, v.shape[2], _io_dtype(q), 0, state.shape[0])
     if out is None:
         out = torch.empty(v.shape, dtype=v.dtype, device=v.device)
     st = load().gdn_recurrent_step_gated(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b),
                                          _ptr(A_log), _ptr(dt_bias), ctypes.c_float(scale), _ptr(state),
-                                         _ptr(state_indices), _ptr(out), _stream(stream))
+                                         _ptr(state_indices), _ptr(z), _ptr(norm_weight),
+                                         ctypes.c_float(norm_eps), _ptr(out), _stream(stream))
     if st != GDN_OK:
         raise GdnError(st, "gdn_recurrent_step_gated")
+    return out
+
+
+def gdn_gated_rmsnorm(o, z, weight, eps, out=None, stream=None):
+    """y = o / sqrt(mean(o^2) + eps) * weight * silu(z) per (token, head) row
+    of o, z [T, Hv, 128] (io dtype) with weight [128] f32. ``out`` may be o."""
+    T, hv, dv = o.shape
+    prob = GdnProblem(1, 0, 1, T, 1, hv, dv, dv, _io_dtype(o), 0, 0)
+    if out is None:
+        out = torch.empty_like(o)
+    st = load().gdn_gated_rmsnorm(ctypes.byref(prob), _ptr(o), _ptr(z), _ptr(weight), ctypes.c_float(eps),
+                                  _ptr(out), _stream(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_gated_rmsnorm")
     return out
 
 

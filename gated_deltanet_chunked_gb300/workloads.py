@@ -16,6 +16,8 @@ Varlen lengths are drawn from the same generator, uniform in [100, 8000].
 Decode front-end inputs (raw projections, nothing normalised):
   q, k  ~ N(0, 1), cast          a, b ~ N(0, 1) (float32, [N, Hv])
   A_log = log U[1, 16]           dt_bias ~ U[-6.9, -2.25]   (float32, [Hv])
+Output gate: z ~ N(0, 1) (io dtype, like v), RMSNorm weight ~ U[0.5, 1.5]
+  (float32, [128]); a stand-alone read-out o ~ N(0, 0.05^2).
 """
 from __future__ import annotations
 
@@ -174,3 +176,15 @@ def make_decode_step_gated(w: Workload, step: int, a_sigma: float = 1.0):
     a = torch.from_numpy(_normal(rng, (N, w.hv), sigma=a_sigma))
     b = torch.from_numpy(_normal(rng, (N, w.hv)))
     return dict(q=q, k=k, v=v, a=a, b=b, scale=1.0 / math.sqrt(DK))
+
+
+def make_output_gate(seed: int, tokens: int, hv: int, io_dtype, with_o: bool = False):
+    """z [tokens, Hv, 128] (io dtype) and the RMSNorm weight [128] f32 of the
+    output gate; with ``with_o`` also a stand-alone read-out o of z's shape."""
+    rng = np.random.Generator(np.random.PCG64([seed, 2]))
+    z = torch.from_numpy(_normal(rng, (tokens, hv, DV))).to(io_dtype)
+    weight = torch.from_numpy(rng.uniform(0.5, 1.5, size=DV).astype(np.float32))
+    if not with_o:
+        return z, weight
+    o = torch.from_numpy(_normal(rng, (tokens, hv, DV), sigma=0.05)).to(io_dtype)
+    return z, weight, o

@@ -192,12 +192,34 @@ int gdn_recurrent_step(const gdn_problem *p, const void *q, const void *k, const
  *             skipped and recorded as GDN_EDEVICE_INPUT).
  * All pointers are caller-owned device memory; q, k, v, out, state and
  * state_indices 16-byte aligned, a, b, A_log, dt_bias 4-byte aligned.
+ *   z, norm_weight, norm_eps: optional output gate. With z non-NULL
+ *             ([num_seqs, hv, 128] io dtype, 16-byte aligned; norm_weight
+ *             [128] f32, 16-byte aligned) out receives
+ *             y = o / sqrt(mean(o^2) + norm_eps) * norm_weight * silu(z)
+ *             per head, computed from the f32 o (as gdn_gated_rmsnorm, but
+ *             without rounding o first); with z NULL out receives o and
+ *             norm_weight is ignored.
  * Returns GDN_EINVAL (nothing launched) on a bad descriptor or pointer.
  * beta is used in f32, without the bf16 rounding of [SGL]'s packed kernel. */
 int gdn_recurrent_step_gated(const gdn_problem *p, const void *q, const void *k, const void *v,
                              const float *a, const float *b, const float *A_log, const float *dt_bias,
                              float scale, float *state, const int32_t *state_indices,
+                             const void *z, const float *norm_weight, float norm_eps,
                              void *out, void *stream);
+
+/* Output gate of the GDN layer ([SGL] node output_rmsnorm_silu_gate; the
+ * gated-RMSNorm row of [Kestrel]): for every token t and v-head h,
+ *   y[t,h] = o[t,h] / sqrt(mean_j o[t,h,j]^2 + eps) * weight * silu(z[t,h])
+ * over the head's 128 channels, normalised before the gate; silu(x) =
+ * x / (1 + exp(-x)); the weight multiplies directly.
+ *   o, z, y  [total_tokens, hv, 128] io dtype (16-byte aligned); y may be o
+ *            (in place)
+ *   weight   [128] f32 (16-byte aligned), shared by the heads
+ *   eps      the RMSNorm epsilon (the pages leave it symbolic)
+ * Only total_tokens, hv, dv and io_dtype of `p` are used (dv must be 128).
+ * Returns GDN_EINVAL (nothing launched) on a bad descriptor or pointer. */
+int gdn_gated_rmsnorm(const gdn_problem *p, const void *o, const void *z, const float *weight, float eps,
+                      void *y, void *stream);
 
 /* Synchronises `stream`, returns the device status word (GDN_OK or the first
  * device-side error recorded since the last clear) and clears it when
@@ -221,7 +243,8 @@ typedef enum gdn_kernel {
     GDN_K_RECURRENT_STEP = 4,     /* decode step */
     GDN_K_CHUNK_FUSED_TC = 5,     /* bf16: chunk preparation and state walk, one co-resident grid (tensor cores) */
     GDN_K_RECURRENT_STEP_GATED = 6, /* decode step with the gate / q-k norm front-end */
-    GDN_K_COUNT = 7
+    GDN_K_GATED_RMSNORM = 7,      /* output gate (head-wise RMSNorm, SiLU(z)) over a whole tensor */
+    GDN_K_COUNT = 8
 } gdn_kernel;
 
 /* Turns per-kernel CUDA-event timing on (non-zero) or off for every later

@@ -111,14 +111,15 @@ def test_recurrent_step_rejects_bad_problems():
     assert step(problem(**ok), idx=FAKE + 4) == gdn.GDN_EINVAL
 
 
+
 def test_recurrent_step_gated_rejects_bad_problems():
     lib = gdn.load()
     P = ctypes.c_void_p
 
-    def step(p, idx=None, ptr=FAKE, gate=FAKE, b=FAKE):
+    def step(p, idx=None, ptr=FAKE, gate=FAKE, b=FAKE, z=None, w=FAKE, eps=1e-6):
         return lib.gdn_recurrent_step_gated(ctypes.byref(p), P(ptr), P(ptr), P(ptr), P(gate), P(b), P(gate),
                                             P(gate), ctypes.c_float(1.0), P(ptr), None if idx is None else P(idx),
-                                            P(ptr), None)
+                                            None if z is None else P(z), P(w), ctypes.c_float(eps), P(ptr), None)
 
     ok = dict(batch=4, seqlen=1, num_seqs=4, total_tokens=4, num_state_slots=4)
     assert step(problem(**{**ok, "num_state_slots": 3})) == gdn.GDN_EINVAL
@@ -129,3 +130,25 @@ def test_recurrent_step_gated_rejects_bad_problems():
     assert step(problem(**ok), gate=FAKE + 2) == gdn.GDN_EINVAL  # gate inputs want 4-byte alignment
     assert step(problem(**ok), b=0) == gdn.GDN_EINVAL
     assert step(problem(**ok), idx=FAKE + 4) == gdn.GDN_EINVAL
+    assert step(problem(**ok), z=FAKE, w=0) == gdn.GDN_EINVAL        # output gate without its weight
+    assert step(problem(**ok), z=FAKE + 2) == gdn.GDN_EINVAL         # misaligned z
+    assert step(problem(**ok), z=FAKE, w=FAKE + 4) == gdn.GDN_EINVAL
+    assert step(problem(**ok), z=FAKE, eps=-1.0) == gdn.GDN_EINVAL
+    assert step(problem(**ok), z=FAKE, eps=float("nan")) == gdn.GDN_EINVAL
+
+
+def test_gated_rmsnorm_rejects_bad_arguments():
+    lib = gdn.load()
+    P = ctypes.c_void_p
+
+    def norm(p, o=FAKE, z=FAKE, w=FAKE, y=FAKE, eps=1e-6):
+        return lib.gdn_gated_rmsnorm(ctypes.byref(p), P(o), P(z), P(w), ctypes.c_float(eps), P(y), None)
+
+    ok = dict(total_tokens=64)
+    assert norm(problem(**{**ok, "dv": 64})) == gdn.GDN_EUNSUPPORTED
+    assert norm(problem(**{**ok, "hv": 0})) == gdn.GDN_EINVAL
+    assert norm(problem(**{**ok, "io_dtype": 5})) == gdn.GDN_EINVAL
+    assert norm(problem(**ok), z=0) == gdn.GDN_EINVAL
+    assert norm(problem(**ok), y=FAKE + 8) == gdn.GDN_EINVAL
+    assert norm(problem(**ok), w=FAKE + 4) == gdn.GDN_EINVAL
+    assert norm(problem(**ok), eps=-1e-3) == gdn.GDN_EINVAL

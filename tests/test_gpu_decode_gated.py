@@ -132,3 +132,42 @@ def test_gated_invalid_arguments(cuda):
                                      d["scale"], state)
     assert e.value.status == gdn.GDN_EINVAL
     assert torch.all(state == 0)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_gated_decode_with_output_gate(cuda, dtype):
+    """Front-end, step and output gate (RMSNorm over the head, silu(z)) in one
+    kernel, against the oracle's step followed by its gated RMSNorm."""
+    w, inp, A_log, dt_bias = _small_case(dtype, N=6, hq=2, hv=4, seed=45)
+    z, weight = W.make_output_gate(45, 6, 4, dtype)
+    idx = torch.tensor([3, 0, -1, 5, 1, 2], dtype=torch.int32)
+    rng = np.random.default_rng(6)
+    state0 = torch.from_numpy(rng.standard_normal((6, 4, 128, 128)).astype(np.float32) * 0.05)
+    state = state0.to(cuda)
+    d = to_dev(inp, cuda)
+    out = torch.full(inp["v"].shape, 7.0, dtype=dtype, device=cuda)
+    gdn.gdn_recurrent_step_gated(d["q"], d["k"], d["v"], d["a"], d["b"], A_log.to(cuda), dt_bias.to(cuda),
+                                 d["scale"], state, state_indices=idx.to(cuda), out=out, z=z.to(cuda),
+                                 norm_weight=weight.to(cuda), norm_eps=1e-6)
+    torch.cuda.synchronize()
+    o_ref, st_ref = step_ref(inp, A_log, dt_bias, state0, idx.numpy())
+    y_ref = oracle.gated_rmsnorm(o_ref, z, weight, 1e-6)
+    live = [0, 1, 3, 4, 5]
+    check(out[live], y_ref[live], dtype, "y")
+    check(state, st_ref, dtype, "state")
+    assert torch.all(out[2] == 7.0)
+
+
+def test_gated_decode_full_with_output_gate(cuda):
+    A_log, dt_bias = W.make_decode_gate_params(DEC)
+    z, weight = W.make_output_gate(DEC.seed, DEC.num_seqs, DEC.hv, DEC.io_dtype)
+    state0 = W.make_decode_state(DEC)
+    state = state0.to(cuda)
+    inp = W.make_decode_step_gated(DEC, 3)
+    d = to_dev(inp, cuda)
+    y = gdn.gdn_recurrent_step_gated(d["q"], d["k"], d["v"], d["a"], d["b"], A_log.to(cuda), dt_bias.to(cuda),
+                                     d["scale"], state, z=z.to(cuda), norm_weight=weight.to(cuda), norm_eps=1e-6)
+    torch.cuda.synchronize()
+    o_ref, st_ref = step_ref(inp, A_log, dt_bias, state0)
+    check(y, oracle.gated_rmsnorm(o_ref, z, weight, 1e-6), torch.bfloat16, "y")
+    check(state, st_ref, torch.bfloat16, "state")
