@@ -288,3 +288,45 @@ def gated_rmsnorm(o, z, weight, eps):
     o, z, weight = _f64(o), _f64(z), _f64(weight)
     rms = np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + float(eps))
     return (o / rms) * weight * silu(z)
+
+
+# ---------------------------------------------------------------------------
+# Short causal convolution with its state ("Kestrel_VLLM-24" page, the
+# conv+SiLU row and kernel: window [s0, s1, s2, x_t] oldest first, the
+# history holding the convolution's INPUTS; "sgl-qwen3-5-moe" page, node 6:
+# x~_{t,c} = SiLU(sum_l w_{c,l} x_{t-l,c} + b_c), a per-channel convolution,
+# b_c = 0 without bias).
+# Weights are stored oldest first, w[c, j] multiplying x_{t-(K-1-j), c}, so the
+# second page's lag-l weight is w[c, K-1-l]. The state of a sequence is its
+# last K-1 inputs, oldest first: [K-1, C].
+# ---------------------------------------------------------------------------
+
+def causal_conv1d_silu(x, weight, bias=None, conv_state=None, cu_seqlens=None, state_indices=None):
+    """x: [T_total, C] packed tokens of the sequences cu_seqlens delimits
+    (one sequence when None); weight: [C, K]; bias: [C] or None;
+    conv_state: [slots, K-1, C] (zeros when None); sequence n uses slot
+    state_indices[n] (n when None; negative: no state in or out, zero history).
+    Returns (out [T_total, C] = SiLU of the convolution, new_state of
+    conv_state's shape, the slots of the sequences replaced by their last K-1
+    inputs)."""
+    x, weight = _f64(x), _f64(weight)
+    T, C = x.shape
+    K = weight.shape[1]
+    b = np.zeros(C) if bias is None else _f64(bias)
+    cu = np.array([0, T]) if cu_seqlens is None else np.asarray(
+        cu_seqlens.detach().cpu().numpy() if hasattr(cu_seqlens, "detach") else cu_seqlens, np.int64)
+    N = len(cu) - 1
+    idx = np.arange(N) if state_indices is None else np.asarray(
+        state_indices.detach().cpu().numpy() if hasattr(state_indices, "detach") else state_indices, np.int64)
+    st = None if conv_state is None else _f64(conv_state).copy()
+    out = np.zeros((T, C))
+    for n in range(N):
+        s, e = int(cu[n]), int(cu[n + 1])
+        hist = st[idx[n]] if (st is not None and idx[n] >= 0) else np.zeros((K - 1, C))
+        ext = np.concatenate([hist, x[s:e]], axis=0)  # [K-1 + L, C], oldest first
+        for t in range(e - s):
+            window = ext[t:t + K]  # x_{t-K+1} .. x_t
+            out[s + t] = silu(np.sum(window * weight.T, axis=0) + b)
+        if st is not None and idx[n] >= 0:
+            st[idx[n]] = ext[ext.shape[0] - (K - 1):]
+    return out, st

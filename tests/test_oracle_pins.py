@@ -17,7 +17,10 @@ against something the pages or plain mathematics fix:
     library cast,
   * the output gate: silu at points with known values, the RMS of a constant
     row and of a one-hot row (a mean, not a sum), norm before gate, per-head
-    normalisation.
+    normalisation,
+  * the short convolution: the impulse response (weight orientation), the
+    history feeding the first outputs, state of short and empty sequences,
+    split/resume, slots and packed sequences, constant input.
 """
 import json
 import math
@@ -478,3 +481,77 @@ def test_gated_rmsnorm_norm_before_gate_and_per_head():
     f = rng.uniform(0.1, 10, (3, 4, 1))
     np.testing.assert_allclose(oracle.gated_rmsnorm(o * f, z1, w, 0.0), oracle.gated_rmsnorm(o, z1, w, 0.0),
                                rtol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# short causal convolution with its state
+# --------------------------------------------------------------------------
+def _silu1(v):
+    return v / (1.0 + math.exp(-v))
+
+
+def test_conv_impulse_response_fixes_orientation():
+    """A unit impulse at t = 0 with zero history: the pre-activation at t is the
+    weight of lag t, w[c, K-1-t] (oldest-first storage), then 0 after K taps."""
+    w = np.array([[0.5, -1.0, 2.0, 3.0], [1.5, 0.25, -0.75, 1.0]])
+    x = np.zeros((6, 2)); x[0] = [1.0, 2.0]
+    out, st = oracle.causal_conv1d_silu(x, w, conv_state=np.zeros((1, 3, 2)))
+    for t in range(6):
+        for c in range(2):
+            pre = x[0, c] * w[c, 3 - t] if t < 4 else 0.0
+            np.testing.assert_allclose(out[t, c], _silu1(pre), rtol=1e-15, atol=1e-300)
+    np.testing.assert_array_equal(st[0], x[3:])  # the last three inputs
+
+
+def test_conv_history_feeds_the_first_outputs():
+    """x = 0 with history [h0, h1, h2]: t = 0 sees w0 h0 + w1 h1 + w2 h2,
+    t = 1 sees w0 h1 + w1 h2, t = 2 sees w0 h2, later outputs are silu(0) = 0;
+    the bias adds to every pre-activation."""
+    w = np.array([[2.0, -3.0, 0.5, 7.0]])
+    h = np.array([[[1.0], [2.0], [-4.0]]])
+    b = np.array([0.25])
+    out, st = oracle.causal_conv1d_silu(np.zeros((5, 1)), w, b, h)
+    pre = [2.0 * 1 - 3.0 * 2 + 0.5 * -4, 2.0 * 2 - 3.0 * -4, 2.0 * -4, 0.0, 0.0]
+    np.testing.assert_allclose(out[:, 0], [_silu1(p + 0.25) for p in pre], rtol=1e-14)
+    np.testing.assert_array_equal(st, np.zeros((1, 3, 1)))
+
+
+def test_conv_short_sequences_keep_part_of_the_old_state():
+    h = np.arange(6, dtype=float).reshape(1, 3, 2)
+    w = np.ones((2, 4))
+    x = np.array([[10.0, 20.0]])
+    _, st1 = oracle.causal_conv1d_silu(x, w, conv_state=h)
+    np.testing.assert_array_equal(st1[0], [[2, 3], [4, 5], [10, 20]])
+    _, st0 = oracle.causal_conv1d_silu(np.zeros((0, 2)), w, conv_state=h, cu_seqlens=[0, 0])
+    np.testing.assert_array_equal(st0, h)  # a zero-length sequence leaves its state
+
+
+def test_conv_split_resume_and_slots():
+    rng = np.random.default_rng(21)
+    C, K = 8, 4
+    w, b = rng.standard_normal((C, K)), rng.standard_normal(C)
+    x = rng.standard_normal((50, C))
+    h = rng.standard_normal((3, K - 1, C))
+    full, st_full = oracle.causal_conv1d_silu(x, w, b, h, [0, 50], [2])
+    a, st_a = oracle.causal_conv1d_silu(x[:17], w, b, h, [0, 17], [2])
+    c, st_c = oracle.causal_conv1d_silu(x[17:], w, b, st_a, [0, 33], [2])
+    np.testing.assert_allclose(np.concatenate([a, c]), full, rtol=1e-14)
+    np.testing.assert_array_equal(st_c, st_full)
+    np.testing.assert_array_equal(st_full[[0, 1]], h[[0, 1]])  # other slots untouched
+    # packed sequences are independent; a negative slot means zero history and no write
+    out2, st2 = oracle.causal_conv1d_silu(x[:30], w, b, h, [0, 12, 30], [-1, 1])
+    o_a, _ = oracle.causal_conv1d_silu(x[:12], w, b, np.zeros((1, K - 1, C)))
+    o_b, s_b = oracle.causal_conv1d_silu(x[12:30], w, b, h[[1]])
+    np.testing.assert_allclose(out2, np.concatenate([o_a, o_b]), rtol=1e-14)
+    np.testing.assert_array_equal(st2[1], s_b[0])
+    np.testing.assert_array_equal(st2[[0, 2]], h[[0, 2]])
+
+
+def test_conv_constant_input():
+    """x = c everywhere, zero history: from t = K-1 on the window is full, so the
+    pre-activation is c sum(w) + b."""
+    w = np.array([[0.1, 0.2, 0.3, 0.4], [1.0, -1.0, 1.0, -1.0]])
+    b = np.array([0.5, -0.5])
+    out, _ = oracle.causal_conv1d_silu(np.full((7, 2), 3.0), w, b)
+    np.testing.assert_allclose(out[3:, 0], _silu1(3.0 * 1.0 + 0.5), rtol=1e-14)
+    np.testing.assert_allclose(out[3:, 1], _silu1(-0.5), rtol=1e-14)
