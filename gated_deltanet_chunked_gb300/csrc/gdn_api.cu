@@ -216,6 +216,43 @@ int gdn_gated_rmsnorm(const gdn_problem *p, const void *o, const void *z, const 
                                             static_cast<cudaStream_t>(stream)));
 }
 
+int gdn_causal_conv1d_silu(const gdn_problem *p, const void *x, const float *weight, const float *bias,
+                           void *conv_state, const int32_t *state_indices, const int32_t *cu_seqlens, int norm_qk,
+                           void *q, void *k, void *v, void *stream) {
+    int st = check_common(p);
+    if (st) return st;
+    if (p->num_seqs < 1 || p->num_state_slots < 0) return GDN_EINVAL;
+    if (!cu_seqlens && p->num_seqs != 1) return GDN_EINVAL;
+    if (conv_state && !state_indices && p->num_state_slots < p->num_seqs) return GDN_EINVAL;
+    // token offsets stay in int (a tile start plus its length), channel blocks in grid.y
+    if (int64_t(p->total_tokens) + 64 >= (int64_t(1) << 31) || (2 * p->hq + p->hv) > 65535 * 8) return GDN_EINVAL;
+    if (!weight || !aligned16(weight) || (bias && !aligned16(bias))) return GDN_EINVAL;
+    if ((conv_state && !aligned16(conv_state)) || (state_indices && !aligned4(state_indices)) ||
+        (cu_seqlens && !aligned4(cu_seqlens)))
+        return GDN_EINVAL;
+    if (p->total_tokens > 0) {
+        if (!x || !q || !k || !v) return GDN_EINVAL;
+        if (!aligned16(x) || !aligned16(q) || !aligned16(k) || !aligned16(v)) return GDN_EINVAL;
+    }
+    int *status = status_ptr();
+    if (!status) return GDN_ECUDA;
+    return cuda_status(launch_conv1d_silu(*p, x, weight, bias, conv_state, state_indices, cu_seqlens, norm_qk, q, k,
+                                          v, status, static_cast<cudaStream_t>(stream)));
+}
+
+int gdn_gating(const gdn_problem *p, const float *a, const float *b, const float *A_log, const float *dt_bias,
+               float *g, float *beta, void *stream) {
+    if (!p || p->hv <= 0 || p->total_tokens < 0) return GDN_EINVAL;
+    const long long n = (long long)p->total_tokens * p->hv;
+    if (n > 0) {
+        if (!a || !b || !A_log || !dt_bias || !g || !beta) return GDN_EINVAL;
+        if (!aligned4(a) || !aligned4(b) || !aligned4(A_log) || !aligned4(dt_bias) || !aligned4(g) ||
+            !aligned4(beta))
+            return GDN_EINVAL;
+    }
+    return cuda_status(launch_gating(a, b, A_log, dt_bias, g, beta, n, p->hv, static_cast<cudaStream_t>(stream)));
+}
+
 int gdn_read_device_status(void *stream, int clear) {
     int *status = status_ptr();
     if (!status) return GDN_ECUDA;

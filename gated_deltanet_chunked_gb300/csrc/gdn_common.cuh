@@ -85,6 +85,11 @@ class LaunchScope {
 
 // Host-side launchers implemented in the kernel translation units.
 cudaError_t launch_chunk_table(const PrefillArgs &a, cudaStream_t s);
+cudaError_t launch_conv1d_silu(const gdn_problem &p, const void *x, const float *weight, const float *bias,
+                               void *conv_state, const int32_t *state_indices, const int32_t *cu_seqlens,
+                               int norm_qk, void *out_q, void *out_k, void *out_v, int *status, cudaStream_t s);
+cudaError_t launch_gating(const float *a, const float *b, const float *A_log, const float *dt_bias, float *g,
+                          float *beta, long long n, int hv, cudaStream_t s);
 cudaError_t launch_gated_rmsnorm(const void *o, const void *z, const float *weight, float eps, void *y,
                                  long long rows, int io_dtype, int *status, cudaStream_t s);
 cudaError_t launch_prefill_simt(const PrefillArgs &a, void *ws_data, cudaStream_t s);
@@ -102,6 +107,13 @@ struct DecodeFront {
     const float *norm_weight;
     float norm_eps;
 };
+
+// log(1 + e^x), linear above 20 and e^x below -20 (no overflow of e^x)
+__device__ __forceinline__ float softplus_f(float x) {
+    if (x > 20.f) return x;
+    if (x < -20.f) return expf(x);
+    return log1pf(expf(x));
+}
 
 // x * sigmoid(x) = x / (1 + e^-x), the output gate's activation. e^-x is
 // taken as 2^(-x log2 e) on the base-2 exponential unit and the quotient

@@ -77,13 +77,6 @@ __device__ __forceinline__ float4 ld4<__nv_bfloat16>(const void *p, size_t i) {
     return make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 
-// log(1 + e^x), linear above 20 and e^x below -20 (no overflow of e^x)
-__device__ __forceinline__ float softplus_f(float x) {
-    if (x > 20.f) return x;
-    if (x < -20.f) return expf(x);
-    return log1pf(expf(x));
-}
-
 template <typename T, bool kFront, bool kGateOut>
 __global__ void __launch_bounds__(kRThreads, 2)
 k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const void *__restrict__ v,

@@ -6,7 +6,8 @@ no fallback: if libgdn.so cannot be built or loaded, ``load()`` raises.
 
 The entry points keep the C names:
   gdn_chunk_fwd, gdn_chunk_fwd_workspace_size, gdn_recurrent_step,
-  gdn_recurrent_step_gated, gdn_gated_rmsnorm, gdn_read_device_status, gdn_status_string, gdn_version.
+  gdn_recurrent_step_gated, gdn_gated_rmsnorm, gdn_causal_conv1d_silu, gdn_gating,
+  gdn_read_device_status, gdn_status_string, gdn_version.
 """
 from __future__ import annotations
 
@@ -24,8 +25,9 @@ GDN_DT_F32, GDN_DT_BF16 = 0, 1
 
 SYMBOLS = ("gdn_chunk_fwd", "gdn_chunk_fwd_workspace_size", "gdn_recurrent_step", "gdn_read_device_status",
            "gdn_status_string", "gdn_version", "gdn_profile_enable", "gdn_profile_collect", "gdn_kernel_name",
-           "gdn_chunk_fwd_noalloc", "gdn_recurrent_step_gated", "gdn_gated_rmsnorm")
-GDN_K_COUNT = 8
+           "gdn_chunk_fwd_noalloc", "gdn_recurrent_step_gated", "gdn_gated_rmsnorm", "gdn_causal_conv1d_silu",
+           "gdn_gating")
+GDN_K_COUNT = 10
 
 
 class GdnProblem(ctypes.Structure):
@@ -64,6 +66,10 @@ def load(path: Optional[str] = None):
                                                      _ip, _vp, _fp, ctypes.c_float, _vp, _vp]
             lib.gdn_gated_rmsnorm.argtypes = [P, _vp, _vp, _fp, ctypes.c_float, _vp, _vp]
             lib.gdn_gated_rmsnorm.restype = ctypes.c_int
+            lib.gdn_causal_conv1d_silu.argtypes = [P, _vp, _fp, _fp, _vp, _ip, _ip, ctypes.c_int, _vp, _vp, _vp, _vp]
+            lib.gdn_causal_conv1d_silu.restype = ctypes.c_int
+            lib.gdn_gating.argtypes = [P, _fp, _fp, _fp, _fp, _fp, _fp, _vp]
+            lib.gdn_gating.restype = ctypes.c_int
             lib.gdn_recurrent_step_gated.restype = ctypes.c_int
             lib.gdn_read_device_status.argtypes = [_vp, ctypes.c_int]
             lib.gdn_read_device_status.restype = ctypes.c_int
@@ -222,6 +228,42 @@ def gdn_gated_rmsnorm(o, z, weight, eps, out=None, stream=None):
     if st != GDN_OK:
         raise GdnError(st, "gdn_gated_rmsnorm")
     return out
+
+
+def gdn_causal_conv1d_silu(x, weight, hq, hv, bias=None, conv_state=None, state_indices=None, cu_seqlens=None,
+                           norm_qk=False, q=None, k=None, v=None, stream=None):
+    """Short causal convolution (4 taps, weight [C, 4] f32 oldest first) + SiLU
+    over packed tokens x [T, C] (C = (2 hq + hv) * 128), split into q, k
+    [T, hq, 128] and v [T, hv, 128]; ``conv_state`` [slots, 3, C] is read and
+    updated in place. ``norm_qk`` L2-normalises every q and k head row."""
+    T, C = x.shape
+    if C != (2 * hq + hv) * 128:
+        raise ValueError("x must have (2 hq + hv) * 128 channels")
+    N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    slots = 0 if conv_state is None else conv_state.shape[0]
+    prob = GdnProblem(1, 0, N, T, hq, hv, 128, 128, _io_dtype(x), 0, slots)
+    q = torch.empty((T, hq, 128), dtype=x.dtype, device=x.device) if q is None else q
+    k = torch.empty((T, hq, 128), dtype=x.dtype, device=x.device) if k is None else k
+    v = torch.empty((T, hv, 128), dtype=x.dtype, device=x.device) if v is None else v
+    st = load().gdn_causal_conv1d_silu(ctypes.byref(prob), _ptr(x), _ptr(weight), _ptr(bias), _ptr(conv_state),
+                                       _ptr(state_indices), _ptr(cu_seqlens), int(bool(norm_qk)), _ptr(q), _ptr(k),
+                                       _ptr(v), _stream(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_causal_conv1d_silu")
+    return q, k, v
+
+
+def gdn_gating(a, b, A_log, dt_bias, g=None, beta=None, stream=None):
+    """g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b), a, b [T, Hv] f32."""
+    T, hv = a.shape
+    prob = GdnProblem(1, 0, 1, T, 1, hv, 128, 128, GDN_DT_F32, 0, 0)
+    g = torch.empty_like(a) if g is None else g
+    beta = torch.empty_like(a) if beta is None else beta
+    st = load().gdn_gating(ctypes.byref(prob), _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(g), _ptr(beta),
+                           _stream(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_gating")
+    return g, beta
 
 
 def gdn_read_device_status(stream=None, clear: bool = True) -> int:

@@ -18,6 +18,9 @@ Decode front-end inputs (raw projections, nothing normalised):
   A_log = log U[1, 16]           dt_bias ~ U[-6.9, -2.25]   (float32, [Hv])
 Output gate: z ~ N(0, 1) (io dtype, like v), RMSNorm weight ~ U[0.5, 1.5]
   (float32, [128]); a stand-alone read-out o ~ N(0, 0.05^2).
+Short convolution: x ~ N(0, 1) (io dtype, [T, (2 Hq + Hv) 128]), weight
+  ~ U[-0.5, 0.5] (float32, [C, 4]), bias ~ N(0, 0.1^2), conv state ~ N(0, 1)
+  (io dtype, [slots, 3, C]).
 """
 from __future__ import annotations
 
@@ -188,3 +191,16 @@ def make_output_gate(seed: int, tokens: int, hv: int, io_dtype, with_o: bool = F
         return z, weight
     o = torch.from_numpy(_normal(rng, (tokens, hv, DV), sigma=0.05)).to(io_dtype)
     return z, weight, o
+
+
+def make_conv_inputs(seed: int, tokens: int, hq: int, hv: int, io_dtype, slots: int = 0, bias: bool = True):
+    """Inputs of the short convolution: x [tokens, C], weight [C, 4], bias [C]
+    (or None) and a conv state [slots, 3, C] (None for slots = 0), with
+    C = (2 hq + hv) * 128."""
+    rng = np.random.Generator(np.random.PCG64([seed, 3]))
+    C = (2 * hq + hv) * DK
+    x = torch.from_numpy(_normal(rng, (tokens, C))).to(io_dtype)
+    weight = torch.from_numpy(rng.uniform(-0.5, 0.5, size=(C, 4)).astype(np.float32))
+    b = torch.from_numpy(_normal(rng, (C,), sigma=0.1)) if bias else None
+    state = torch.from_numpy(_normal(rng, (slots, 3, C))).to(io_dtype) if slots else None
+    return x, weight, b, state

@@ -221,6 +221,50 @@ int gdn_recurrent_step_gated(const gdn_problem *p, const void *q, const void *k,
 int gdn_gated_rmsnorm(const gdn_problem *p, const void *o, const void *z, const float *weight, float eps,
                       void *y, void *stream);
 
+/* Short causal depthwise convolution + SiLU with its state, and the split of
+ * its output into q, k, v ([Kestrel] conv+SiLU row: window [s0, s1, s2, x_t]
+ * oldest first, the state holding the convolution's inputs; [SGL] node 6:
+ * x~[t,c] = SiLU(sum_l w[c,l] x[t-l,c] + b[c]), and its layout step).
+ * Channels c < C = (2 hq + hv) * 128, taps K = 4, for every packed token t
+ * of sequence n (cu_seqlens) at position p:
+ *   y[t,c] = SiLU(bias[c] + sum_j weight[c,j] * e[p + j, c]),  j = 0 .. 3,
+ * where e = [state of n (3 rows, oldest first) ; the sequence's inputs x], so
+ * weight[c,3] multiplies x[t] and weight[c,0] the input three steps back
+ * ([SGL]'s lag-l weight is weight[c, 3 - l]). Then q[t] = y[t, 0 : hq*128),
+ * k[t] = y[t, hq*128 : 2*hq*128), v[t] = y[t, 2*hq*128 : C), each as
+ * [hq or hv, 128] rows; with norm_qk != 0 each q and k head row is divided
+ * by sqrt(its sum of squares + 1e-6) ([SGL] node 7 step one, without the
+ * query scale). The state of sequence n becomes the last 3 rows of e (the
+ * last three inputs; part of the old state when the sequence is shorter).
+ *   x          [total_tokens, C] io dtype, 16-byte aligned
+ *   weight     [C, 4] f32, bias [C] f32 or NULL (zero), 16-byte aligned
+ *   conv_state [num_state_slots, 3, C] io dtype, read and written in place,
+ *              or NULL (zero history, nothing written)
+ *   state_indices int32 [num_seqs] or NULL (sequence n uses slot n); a
+ *              negative index means zero history and no state write; an
+ *              index >= num_state_slots is treated the same and recorded as
+ *              GDN_EDEVICE_INPUT
+ *   cu_seqlens int32 [num_seqs + 1] packed offsets (checked on the device),
+ *              or NULL for one sequence of total_tokens (num_seqs must be 1).
+ *              Decode: one token per sequence, cu_seqlens = 0, 1, ..., N.
+ *   q, k       [total_tokens, hq, 128], v [total_tokens, hv, 128], io dtype
+ * Two sequences must not name the same slot. Returns GDN_EINVAL (nothing
+ * launched) on a bad descriptor or pointer. */
+int gdn_causal_conv1d_silu(const gdn_problem *p, const void *x, const float *weight, const float *bias,
+                           void *conv_state, const int32_t *state_indices, const int32_t *cu_seqlens,
+                           int norm_qk, void *q, void *k, void *v, void *stream);
+
+/* Gates of every token from the gate projections ([SGL] gdn_gating node;
+ * [Kestrel] gating kernel, softplus linear above 20 and exponential below
+ * -20): for t < total_tokens, h < hv,
+ *   g[t,h] = -exp(A_log[h]) * softplus(a[t,h] + dt_bias[h]),
+ *   beta[t,h] = 1 / (1 + exp(-b[t,h])),
+ * ready for gdn_chunk_fwd (g is the raw per-token log-decay).
+ *   a, b, g, beta [total_tokens, hv] f32; A_log, dt_bias [hv] f32; all
+ *   4-byte aligned. */
+int gdn_gating(const gdn_problem *p, const float *a, const float *b, const float *A_log, const float *dt_bias,
+               float *g, float *beta, void *stream);
+
 /* Synchronises `stream`, returns the device status word (GDN_OK or the first
  * device-side error recorded since the last clear) and clears it when
  * `clear` is non-zero. Returns GDN_ECUDA if the CUDA calls themselves fail. */
@@ -244,7 +288,9 @@ typedef enum gdn_kernel {
     GDN_K_CHUNK_FUSED_TC = 5,     /* bf16: chunk preparation and state walk, one co-resident grid (tensor cores) */
     GDN_K_RECURRENT_STEP_GATED = 6, /* decode step with the gate / q-k norm front-end */
     GDN_K_GATED_RMSNORM = 7,      /* output gate (head-wise RMSNorm, SiLU(z)) over a whole tensor */
-    GDN_K_COUNT = 8
+    GDN_K_CONV1D_SILU = 8,        /* short causal convolution + SiLU with conv state, split into q, k, v */
+    GDN_K_GATING = 9,             /* g and beta from the gate projections, every token */
+    GDN_K_COUNT = 10
 } gdn_kernel;
 
 /* Turns per-kernel CUDA-event timing on (non-zero) or off for every later

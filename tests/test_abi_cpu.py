@@ -152,3 +152,31 @@ def test_gated_rmsnorm_rejects_bad_arguments():
     assert norm(problem(**ok), y=FAKE + 8) == gdn.GDN_EINVAL
     assert norm(problem(**ok), w=FAKE + 4) == gdn.GDN_EINVAL
     assert norm(problem(**ok), eps=-1e-3) == gdn.GDN_EINVAL
+
+
+def test_conv_and_gating_reject_bad_arguments():
+    lib = gdn.load()
+    P = ctypes.c_void_p
+
+    def conv(p, x=FAKE, w=FAKE, b=None, st=None, idx=None, cu=FAKE, out=FAKE):
+        return lib.gdn_causal_conv1d_silu(ctypes.byref(p), P(x), P(w), None if b is None else P(b),
+                                          None if st is None else P(st), None if idx is None else P(idx),
+                                          None if cu is None else P(cu), 0, P(out), P(out), P(out), None)
+
+    ok = dict(batch=1, seqlen=0, num_seqs=2, total_tokens=64, hq=1, hv=2, num_state_slots=2)
+    assert conv(problem(**{**ok, "dk": 64, "dv": 64})) == gdn.GDN_EUNSUPPORTED
+    assert conv(problem(**{**ok, "num_seqs": 0})) == gdn.GDN_EINVAL
+    assert conv(problem(**ok), cu=None) == gdn.GDN_EINVAL            # two sequences need offsets
+    assert conv(problem(**{**ok, "num_state_slots": 1}), st=FAKE) == gdn.GDN_EINVAL  # identity slots
+    assert conv(problem(**ok), w=0) == gdn.GDN_EINVAL
+    assert conv(problem(**ok), w=FAKE + 4) == gdn.GDN_EINVAL
+    assert conv(problem(**ok), b=FAKE + 8) == gdn.GDN_EINVAL
+    assert conv(problem(**ok), x=FAKE + 2) == gdn.GDN_EINVAL
+    assert conv(problem(**ok), cu=FAKE + 2) == gdn.GDN_EINVAL
+
+    def gating(p, a=FAKE, g=FAKE):
+        return lib.gdn_gating(ctypes.byref(p), P(a), P(a), P(a), P(a), P(g), P(g), None)
+
+    assert gating(problem(hv=0)) == gdn.GDN_EINVAL
+    assert gating(problem(), a=0) == gdn.GDN_EINVAL
+    assert gating(problem(), g=FAKE + 2) == gdn.GDN_EINVAL

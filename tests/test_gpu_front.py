@@ -1,0 +1,156 @@
+"""Parity of the front-end kernels (CUDA, through the C ABI) with the oracle:
+the short causal convolution + SiLU with its state and the q/k/v split
+(gdn_causal_conv1d_silu), the gates of every token (gdn_gating), and the
+prefill layer core from raw projections to the gated output
+(conv -> gating -> chunk form -> output gate).
+
+Convolution cases: packed sequences of lengths 0 to 150 (shorter than the
+window, empty, spanning token tiles), slot indices with a padding slot, no
+state, the fused q/k norm, 20 chained decode steps of 256 sequences, and one
+4096-token sequence of 8192 channels.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_deltanet_chunked_gb300 import gdn, workloads as W
+from parity_util import check
+
+pytestmark = pytest.mark.gpu
+
+
+def split_ref(y, hq, hv):
+    T = y.shape[0]
+    q = y[:, :hq * 128].reshape(T, hq, 128)
+    k = y[:, hq * 128:2 * hq * 128].reshape(T, hq, 128)
+    v = y[:, 2 * hq * 128:].reshape(T, hv, 128)
+    return q, k, v
+
+
+def run_conv(dev, x, w, b, st, idx, cu, hq, hv, norm=False):
+    d = lambda t: None if t is None else t.to(dev)
+    out = gdn.gdn_causal_conv1d_silu(d(x), d(w), hq, hv, bias=d(b), conv_state=st, state_indices=d(idx),
+                                     cu_seqlens=d(cu), norm_qk=norm)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("norm", [False, True], ids=["raw", "qknorm"])
+def test_conv_packed_sequences_with_slots(cuda, dtype, norm):
+    lengths = [150, 2, 0, 1, 70, 3, 33]
+    hq, hv = 2, 4
+    T = sum(lengths)
+    x, w, b, st0 = W.make_conv_inputs(61, T, hq, hv, dtype, slots=8)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32)
+    idx = torch.tensor([4, 0, 7, -1, 2, 1, 6], dtype=torch.int32)
+    st = st0.to(cuda)
+    gdn.gdn_read_device_status(clear=True)
+    q, k, v = run_conv(cuda, x, w, b, st, idx, cu, hq, hv, norm)
+    assert gdn.gdn_read_device_status() == gdn.GDN_OK
+    y_ref, st_ref = oracle.causal_conv1d_silu(x, w, b, st0, cu, idx)
+    q_ref, k_ref, v_ref = split_ref(y_ref, hq, hv)
+    if norm:
+        q_ref, k_ref = oracle.l2_normalise(q_ref), oracle.l2_normalise(k_ref)
+    for name, got, ref in (("q", q, q_ref), ("k", k, k_ref), ("v", v, v_ref)):
+        check(got, ref, dtype, name)
+    check(st, st_ref, dtype, "conv state")
+    assert torch.equal(st[[3, 5]], st0[[3, 5]].to(cuda))  # slots nobody names
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_conv_without_state_one_sequence(cuda, dtype):
+    x, w, b, _ = W.make_conv_inputs(62, 300, 1, 2, dtype)
+    q, k, v = run_conv(cuda, x, w, None, None, None, None, 1, 2)
+    y_ref, _ = oracle.causal_conv1d_silu(x, w)
+    for got, ref in zip((q, k, v), split_ref(y_ref, 1, 2)):
+        check(got, ref, dtype, "y")
+
+
+def test_conv_decode_steps_chained(cuda):
+    """256 sequences of one token each, 20 steps, state slots permuted."""
+    hq, hv, N = 16, 32, 256
+    _, w, b, st0 = W.make_conv_inputs(63, 1, hq, hv, torch.bfloat16, slots=N)
+    idx = torch.from_numpy(np.random.default_rng(3).permutation(N).astype(np.int32))
+    cu = torch.arange(N + 1, dtype=torch.int32)
+    st = st0.to(cuda)
+    st_ref = st0.double().numpy()
+    for step in range(20):
+        x, _, _, _ = W.make_conv_inputs(1000 + step, N, hq, hv, torch.bfloat16)
+        q, k, v = run_conv(cuda, x, w, b, st, idx, cu, hq, hv)
+        y_ref, st_ref = oracle.causal_conv1d_silu(x, w, b, st_ref, cu, idx)
+        if step in (0, 19):
+            for got, ref in zip((q, k, v), split_ref(y_ref, hq, hv)):
+                check(got, ref, torch.bfloat16, f"y step {step}")
+    check(st, st_ref, torch.bfloat16, "conv state after 20 steps")
+
+
+def test_conv_prefill_size(cuda):
+    """One 4096-token sequence, Hq = 16, Hv = 32 (8192 channels), bf16, with state."""
+    hq, hv = 16, 32
+    x, w, b, st0 = W.make_conv_inputs(64, 4096, hq, hv, torch.bfloat16, slots=1)
+    st = st0.to(cuda)
+    q, k, v = run_conv(cuda, x, w, b, st, None, torch.tensor([0, 4096], dtype=torch.int32), hq, hv, norm=True)
+    y_ref, st_ref = oracle.causal_conv1d_silu(x, w, b, st0)
+    q_ref, k_ref, v_ref = split_ref(y_ref, hq, hv)
+    check(q, oracle.l2_normalise(q_ref), torch.bfloat16, "q")
+    check(k, oracle.l2_normalise(k_ref), torch.bfloat16, "k")
+    check(v, v_ref, torch.bfloat16, "v")
+    check(st, st_ref, torch.bfloat16, "conv state")
+
+
+def test_conv_bad_offsets_report_status(cuda):
+    x, w, b, _ = W.make_conv_inputs(65, 10, 1, 2, torch.float32)
+    cu = torch.tensor([0, 6, 4, 10], dtype=torch.int32)  # decreasing: rejected on the device
+    gdn.gdn_read_device_status(clear=True)
+    run_conv(cuda, x, w, b, None, None, cu, 1, 2)
+    assert gdn.gdn_read_device_status(clear=True) == gdn.GDN_EDEVICE_INPUT
+
+
+def test_gating_every_token(cuda):
+    rng = np.random.default_rng(66)
+    T, hv = 1000, 32
+    a = torch.from_numpy((rng.standard_normal((T, hv)) * 15).astype(np.float32))  # both softplus branches
+    b = torch.from_numpy((rng.standard_normal((T, hv)) * 30).astype(np.float32))
+    w = W.WORKLOADS["decode_N256_hq16_hv32"]
+    A_log, dt_bias = W.make_decode_gate_params(w)
+    g, beta = gdn.gdn_gating(a.to(cuda), b.to(cuda), A_log.to(cuda), dt_bias.to(cuda))
+    torch.cuda.synchronize()
+    g_ref, beta_ref = oracle.decode_gates(a, b, A_log, dt_bias)
+    check(g, g_ref, torch.float32, "g")
+    check(beta, beta_ref, torch.float32, "beta")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_prefill_layer_core_from_projections(cuda, dtype):
+    """conv (+ q/k norm) -> gates -> chunk form -> output gate, against the
+    oracle's convolution, L2 norm, gates, chunk form and gated RMSNorm."""
+    lengths, hq, hv = [100, 37, 64], 1, 2
+    T = sum(lengths)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32)
+    x, w, b, st0 = W.make_conv_inputs(67, T, hq, hv, dtype, slots=3)
+    rng = np.random.default_rng(68)
+    a = torch.from_numpy(rng.standard_normal((T, hv)).astype(np.float32))
+    bb = torch.from_numpy(rng.standard_normal((T, hv)).astype(np.float32))
+    wl = W.Workload("layer", 68, "decode", dtype, hq=hq, hv=hv)
+    A_log, dt_bias = W.make_decode_gate_params(wl)
+    z, nw = W.make_output_gate(68, T, hv, dtype)
+    scale = 128 ** -0.5
+    # CUDA path
+    st = st0.to(cuda)
+    q, k, v = run_conv(cuda, x, w, b, st, None, cu, hq, hv, norm=True)
+    g, beta = gdn.gdn_gating(a.to(cuda), bb.to(cuda), A_log.to(cuda), dt_bias.to(cuda))
+    o, S = gdn.gdn_chunk_fwd(q, k, v, g, beta, scale, cu_seqlens=cu.to(cuda))
+    y = gdn.gdn_gated_rmsnorm(o, z.to(cuda), nw.to(cuda), 1e-6)
+    torch.cuda.synchronize()
+    assert gdn.gdn_read_device_status() == gdn.GDN_OK
+    # oracle chain
+    y_c, st_ref = oracle.causal_conv1d_silu(x, w, b, st0, cu)
+    q_r, k_r, v_r = split_ref(y_c, hq, hv)
+    g_r, beta_r = oracle.decode_gates(a, bb, A_log, dt_bias)
+    o_r, S_r = oracle.chunked(oracle.l2_normalise(q_r), oracle.l2_normalise(k_r), v_r, g_r, beta_r, scale,
+                              None, cu.numpy())
+    check(y, oracle.gated_rmsnorm(o_r, z, nw, 1e-6), dtype, "y")
+    check(S, S_r, dtype, "final state")
+    check(st, st_ref, dtype, "conv state")
