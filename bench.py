@@ -12,7 +12,8 @@ v-heads, f32 state read and written in place) is measured in the same run and
 reported under "decode"; the same step fed raw q/k and gate projections (the
 front-end and the output gate computed in the kernel) under "decode_gated";
 the stand-alone output gate (gdn_gated_rmsnorm) over the prefill's
-[4096, 32, 128] read-out under "output_gate".
+[4096, 32, 128] read-out under "output_gate"; the short convolution (prefill
+projections and one decode step) and the gating under "front_end".
 
 Multi-GPU (torchrun, one rank per GPU): every rank runs its own replica of the
 workload (weak scaling: the GDN core shards over sequences and heads with no
@@ -373,6 +374,7 @@ def run_ours(args, world, rank, local):
     decode = None if args.no_decode else run_decode(args, dev, world, peaks, peak_src)
     decode_gated = None if args.no_decode else run_decode(args, dev, world, peaks, peak_src, gated=True)
     output_gate = None if args.no_decode else run_gate_norm(args, dev, world, peaks, peak_src)
+    front_end = None if args.no_decode else run_front_end(args, dev, world, peaks, peak_src)
     clocks.stop()
     clk = clocks.summary(t_start, t_end)
 
@@ -389,6 +391,7 @@ def run_ours(args, world, rank, local):
                    "l2": L2_NOTE, "parallelism": f"replicas x{world}"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": gpu_launches,
         "kernels": kernels, "decode": decode, "decode_gated": decode_gated, "output_gate": output_gate,
+        "front_end": front_end,
         "step_ms": {"median": statistics.median(step_ms), "p10": sorted(step_ms)[len(step_ms) // 10],
                     "p90": sorted(step_ms)[(9 * len(step_ms)) // 10]},
     }
@@ -503,6 +506,77 @@ def run_gate_norm(args, dev, world, peaks, peak_src):
                      "peak_source": f"{peak_src} (hbm_gbs, burst copy)"},
         "l2": "inputs rotate over 4 sets of o, z, y (403 MB, larger than L2); no flush",
     }
+
+
+def run_front_end(args, dev, world, peaks, peak_src):
+    """Times the short convolution (gdn_causal_conv1d_silu, q/k norm fused) on
+    the prefill workload's projections (T = 4096, C = 8192 bf16, with state)
+    and on one decode step (256 sequences), and the per-token gating, each
+    rotating over input sets larger than L2."""
+    from gated_deltanet_chunked_gb300 import gdn
+
+    res = {}
+    hq, hv = PREFILL.hq, PREFILL.hv
+    for name, T, N in (("conv_prefill_T4096", PREFILL.seqlen, 1), ("conv_decode_N256", DECODE.num_seqs,
+                                                                    DECODE.num_seqs)):
+        nsets = 4 if N == 1 else 16
+        sets = []
+        for i in range(nsets):
+            x, w, b, st = W.make_conv_inputs(7000 + i, T, hq, hv, PREFILL.io_dtype, slots=N)
+            cu = torch.arange(N + 1, dtype=torch.int32) if N > 1 else torch.tensor([0, T], dtype=torch.int32)
+            q = torch.empty((T, hq, 128), dtype=x.dtype, device=dev)
+            k, v = torch.empty_like(q), torch.empty((T, hv, 128), dtype=x.dtype, device=dev)
+            sets.append([t.to(dev) for t in (x, w, b, st, cu)] + [q, k, v])
+
+        def launch(i):
+            x, w, b, st, cu, q, k, v = sets[i % nsets]
+            if N > 1:  # one token per sequence: the decode step kernel
+                gdn.gdn_causal_conv1d_silu_step(x, w, hq, hv, bias=b, conv_state=st, norm_qk=True, q=q, k=k, v=v)
+            else:
+                gdn.gdn_causal_conv1d_silu(x, w, hq, hv, bias=b, conv_state=st, cu_seqlens=cu, norm_qk=True,
+                                           q=q, k=k, v=v)
+        for i in range(max(3, args.warmup)):
+            launch(i)
+        steps = max(16, min(args.steps, 100))
+        gdn.gdn_profile_collect(reset=True)
+        gdn.gdn_profile_enable(True)
+        torch.cuda.synchronize()
+        for i in range(steps):
+            launch(i)
+        torch.cuda.synchronize()
+        gdn.gdn_profile_enable(False)
+        prof = gdn.gdn_profile_collect(reset=True)
+        kname = "conv1d_step" if N > 1 else "conv1d_silu"
+        _, kms, nt = prof.get(kname, (0, 0.0, 0))
+        k_ms = max_over_ranks(kms / max(nt, 1), world, dev)
+        C = (2 * hq + hv) * 128
+        # x in, q/k/v out (bf16); conv state 3 rows read + written per sequence; weight and bias (f32)
+        total = 2 * T * C * 2 + 2 * N * 3 * C * 2 + C * 4 * 4 + C * 4
+        res[name] = {"ms_per_launch": k_ms, "bytes_per_launch": total,
+                     "roofline": {"kernel": kname, "bound": "hbm", "achieved": total / (k_ms * 1e-3) / 1e9,
+                                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": total / (k_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+                     "l2": f"inputs rotate over {nsets} sets; no flush"}
+        del sets
+    # gating of every token of the prefill workload ([4096, 32] a, b in; g, beta out)
+    T = PREFILL.seqlen
+    A_log, dt_bias = (t.to(dev) for t in W.make_decode_gate_params(DECODE))
+    gs = [tuple(torch.randn((T, hv), device=dev) for _ in range(4)) for _ in range(4)]
+    for i in range(3):
+        a, b, g, beta = gs[i % 4]
+        gdn.gdn_gating(a, b, A_log, dt_bias, g=g, beta=beta)
+    gdn.gdn_profile_collect(reset=True)
+    gdn.gdn_profile_enable(True)
+    for i in range(20):
+        a, b, g, beta = gs[i % 4]
+        gdn.gdn_gating(a, b, A_log, dt_bias, g=g, beta=beta)
+    torch.cuda.synchronize()
+    gdn.gdn_profile_enable(False)
+    _, kms, nt = gdn.gdn_profile_collect(reset=True).get("gating", (0, 0.0, 0))
+    res["gating_T4096"] = {"ms_per_launch": max_over_ranks(kms / max(nt, 1), world, dev),
+                           "bytes_per_launch": 4 * T * hv * 4, "bound": "launch (2 MB per launch)"}
+    res["peak_source"] = f"{peak_src} (hbm_gbs, burst copy)"
+    return res
 
 
 def cpu_baseline(host, w, fraction):

@@ -240,6 +240,26 @@ int gdn_causal_conv1d_silu(const gdn_problem *p, const void *x, const float *wei
                                           v, status, static_cast<cudaStream_t>(stream)));
 }
 
+int gdn_causal_conv1d_silu_step(const gdn_problem *p, const void *x, const float *weight, const float *bias,
+                                void *conv_state, const int32_t *state_indices, int norm_qk, void *q, void *k,
+                                void *v, void *stream) {
+    int st = check_common(p);
+    if (st) return st;
+    if (p->num_seqs < 0 || p->total_tokens != p->num_seqs || p->num_state_slots < 0) return GDN_EINVAL;
+    if (conv_state && !state_indices && p->num_state_slots < p->num_seqs) return GDN_EINVAL;
+    if ((2 * p->hq + p->hv) > 65535 * 8) return GDN_EINVAL;
+    if (!weight || !aligned16(weight) || (bias && !aligned16(bias))) return GDN_EINVAL;
+    if ((conv_state && !aligned16(conv_state)) || (state_indices && !aligned4(state_indices))) return GDN_EINVAL;
+    if (p->num_seqs > 0) {
+        if (!x || !q || !k || !v) return GDN_EINVAL;
+        if (!aligned16(x) || !aligned16(q) || !aligned16(k) || !aligned16(v)) return GDN_EINVAL;
+    }
+    int *status = status_ptr();
+    if (!status) return GDN_ECUDA;
+    return cuda_status(launch_conv1d_step(*p, x, weight, bias, conv_state, state_indices, norm_qk, q, k, v, status,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
 int gdn_gating(const gdn_problem *p, const float *a, const float *b, const float *A_log, const float *dt_bias,
                float *g, float *beta, void *stream) {
     if (!p || p->hv <= 0 || p->total_tokens < 0) return GDN_EINVAL;

@@ -88,6 +88,9 @@ cudaError_t launch_chunk_table(const PrefillArgs &a, cudaStream_t s);
 cudaError_t launch_conv1d_silu(const gdn_problem &p, const void *x, const float *weight, const float *bias,
                                void *conv_state, const int32_t *state_indices, const int32_t *cu_seqlens,
                                int norm_qk, void *out_q, void *out_k, void *out_v, int *status, cudaStream_t s);
+cudaError_t launch_conv1d_step(const gdn_problem &p, const void *x, const float *weight, const float *bias,
+                               void *conv_state, const int32_t *state_indices, int norm_qk, void *out_q,
+                               void *out_k, void *out_v, int *status, cudaStream_t s);
 cudaError_t launch_gating(const float *a, const float *b, const float *A_log, const float *dt_bias, float *g,
                           float *beta, long long n, int hv, cudaStream_t s);
 cudaError_t launch_gated_rmsnorm(const void *o, const void *z, const float *weight, float eps, void *y,

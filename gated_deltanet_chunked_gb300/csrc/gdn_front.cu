@@ -6,6 +6,8 @@
 //    sgl-qwen3-5-moe page's node 6 with the split of its output into q, k, v),
 //    optionally followed by the per-head L2 norm of q and k (decode node 7,
 //    step one, without the query scale, which the chunk form applies).
+//  k_conv1d_step -- the same for one token per sequence (decode), the state
+//    shifted in place by the thread that owns the channels.
 //  k_gating -- g = -exp(A_log) softplus(a + dt_bias) and beta = sigmoid(b) for
 //    every token (the sgl-qwen3-5-moe page's gdn_gating node; the softplus
 //    branches of the Kestrel page's gating kernel).
@@ -16,14 +18,20 @@
 // access per token), so a warp covers exactly one 128-channel head and the
 // q/k norm is one warp reduction. A CTA (grid x: token tiles, y: channel
 // blocks) takes 1024 channels over a tile of tokens of the packed token axis
-// and slides the window down it in registers; tiles may span several
-// sequences (the window restarts from each sequence's state).
+// and slides the window down it in registers. The tile's rows of x (2 KiB per
+// token for bf16) come into shared memory by bulk copies issued at once by one
+// thread, so that a whole tile is in flight per CTA without holding
+// registers (loads issued token by token left the kernel bound by load
+// latency at 0.3 of HBM); tiles may span several sequences (the window
+// restarts from each sequence's state). A token that is a whole sequence
+// (decode) finds its sequence without a search.
 // In-place state update without a race: a tile never starts at the second or
 // third token of a sequence (its start moves to the fourth), so the old state
 // of a sequence is read only by the thread that processes the sequence's
 // first token, and that same thread writes the new state (the last K-1
 // inputs) after it has read the old one.
 #include "gdn_common.cuh"
+#include "tc_ptx.cuh"
 
 namespace gdn {
 namespace {
@@ -32,6 +40,7 @@ constexpr int kConvK = 4;  // taps
 constexpr int kCThreads = 256;
 constexpr int kCPerThread = 4;
 constexpr int kCPerBlock = kCThreads * kCPerThread;  // 1024 channels
+constexpr int kMaxTileBytes = 64 * 1024;            // x rows staged per CTA (plus two rows)
 
 template <typename T>
 __device__ __forceinline__ float4 ld4v(const T *p);
@@ -69,6 +78,7 @@ struct ConvArgs {
 
 // sequence holding token t (cu[s] <= t < cu[s+1]); the last non-empty one for t = T
 __device__ __forceinline__ int seq_of(const int32_t *cu, int N, int t) {
+    if (t < N && cu[t] == t && cu[t + 1] == t + 1) return t;  // one token per sequence (decode)
     int lo = 0, hi = N - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -90,6 +100,10 @@ __device__ __forceinline__ int tile_start(const int32_t *cu, int N, int T, int t
 
 template <typename T>
 __global__ void __launch_bounds__(kCThreads) k_conv1d_silu(ConvArgs a) {
+    using namespace tc;
+    extern __shared__ __align__(128) uint8_t xs_raw[];  // the tile's rows of x: [rows][1024] T
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
     const int lane = threadIdx.x & 31;
     const int c0 = blockIdx.y * kCPerBlock + threadIdx.x * kCPerThread;
     const int32_t one_seq[2] = {0, a.T};
@@ -104,13 +118,30 @@ __global__ void __launch_bounds__(kCThreads) k_conv1d_silu(ConvArgs a) {
             return;
         }
     }
-    if (c0 >= a.C) return;  // whole warps: C is a multiple of 128
     const int t_nominal = int(blockIdx.x) * a.tile;
     const int t_begin = tile_start(cu, N, a.T, t_nominal);
     const int t_end = tile_start(cu, N, a.T, min(t_nominal + a.tile, a.T));
-    if (t_begin >= t_end) return;
+    if (t_begin >= t_end) return;  // uniform over the CTA
     const T *X = static_cast<const T *>(a.x);
+    // the tile's rows of x for these 1024 channels, by bulk copies (one per token)
+    const int cb0 = blockIdx.y * kCPerBlock;
+    const uint32_t row_bytes = uint32_t(min(kCPerBlock, a.C - cb0)) * sizeof(T);
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+        mbar_arrive_expect_tx(&bar, uint32_t(t_end - t_begin) * row_bytes);
+        for (int t = t_begin; t < t_end; ++t)
+            bulk_load(xs_raw + size_t(t - t_begin) * kCPerBlock * sizeof(T), X + size_t(t) * a.C + cb0, row_bytes,
+                      &bar);
+    }
+    __syncthreads();
+    const bool active = c0 < a.C;  // whole warps: C is a multiple of 128
     T *S = static_cast<T *>(a.state);
+    if (!active) {  // still waits for the copies into this CTA's shared memory
+        if (threadIdx.x == 0 && !mbar_wait(&bar, 0)) record_status(a.status, GDN_ETIMEOUT);
+        return;
+    }
     float4 w[kConvK];  // w[j] = taps j of the 4 channels
     {
         float4 r[kCPerThread];
@@ -160,19 +191,15 @@ __global__ void __launch_bounds__(kCThreads) k_conv1d_silu(ConvArgs a) {
 #pragma unroll
             for (int i = 0; i < kConvK - 1; ++i) {
                 const int j = L + i;  // last K-1 entries of [state ; x]
-                const float4 v = j >= kConvK - 1 ? ld4v<T>(X + size_t(ss + j - (kConvK - 1)) * a.C + c0) : e[j];
+                const float4 v = j >= kConvK - 1 ? ld4v<T>(X + size_t(ss + j - (kConvK - 1)) * a.C + c0)
+                                 : j == 0          ? e[0]
+                                 : j == 1          ? e[1]
+                                                   : e[2];
                 st4v<T>(S + (size_t(slot) * (kConvK - 1) + i) * a.C + c0, v);
             }
         }
     };
-    load_history(t_begin);
-    for (int t = t_begin; t < t_end; ++t) {
-        if (t == s_end) {  // next non-empty sequence starts here
-            while (cu[s + 1] <= t) ++s;
-            s_end = cu[s + 1];
-            load_history(t);
-        }
-        const float4 xv = ld4v<T>(X + size_t(t) * a.C + c0);
+    auto emit = [&](int t, const float4 &xv) {
         float4 y;
         y.x = silu_f(fmaf(w[3].x, xv.x, fmaf(w[2].x, h2.x, fmaf(w[1].x, h1.x, fmaf(w[0].x, h0.x, bias.x)))));
         y.y = silu_f(fmaf(w[3].y, xv.y, fmaf(w[2].y, h2.y, fmaf(w[1].y, h1.y, fmaf(w[0].y, h0.y, bias.y)))));
@@ -186,6 +213,67 @@ __global__ void __launch_bounds__(kCThreads) k_conv1d_silu(ConvArgs a) {
         }
         st4v<T>(dst + size_t(t) * drow + dcol, y);
         h0 = h1, h1 = h2, h2 = xv;
+    };
+    load_history(t_begin);
+    const bool landed = mbar_wait(&bar, 0);
+    if (!__all_sync(0xffffffffu, landed)) {
+        if (lane == 0) record_status(a.status, GDN_ETIMEOUT);
+        return;
+    }
+    const T *XS = reinterpret_cast<const T *>(xs_raw) + threadIdx.x * kCPerThread;
+    for (int t = t_begin; t < t_end;) {
+        if (t == s_end) {  // next non-empty sequence starts here
+            while (cu[s + 1] <= t) ++s;
+            s_end = cu[s + 1];
+            load_history(t);
+        }
+        const int run_end = min(t_end, s_end);  // tokens of sequence s in this tile
+        for (; t < run_end; ++t) emit(t, ld4v<T>(XS + size_t(t - t_begin) * kCPerBlock));
+    }
+}
+
+// One token per sequence (decode): block (n, channel block); the token's x
+// and the sequence's slot are read at once, then the three state rows.
+template <typename T>
+__global__ void __launch_bounds__(kCThreads) k_conv1d_step(ConvArgs a) {
+    const int n = blockIdx.x;
+    const int c0 = blockIdx.y * kCPerBlock + threadIdx.x * kCPerThread;
+    if (c0 >= a.C) return;  // whole warps
+    const T *X = static_cast<const T *>(a.x);
+    T *S = static_cast<T *>(a.state);
+    int slot = S ? (a.idx ? a.idx[n] : n) : -1;
+    const float4 xv = ld4v<T>(X + size_t(n) * a.C + c0);
+    float4 r[kCPerThread];
+#pragma unroll
+    for (int i = 0; i < kCPerThread; ++i) r[i] = reinterpret_cast<const float4 *>(a.weight)[c0 + i];
+    const float4 bias = a.bias ? *reinterpret_cast<const float4 *>(a.bias + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (slot >= a.slots) {
+        if ((threadIdx.x & 31) == 0) record_status(a.status, GDN_EDEVICE_INPUT);
+        slot = -1;
+    }
+    float4 h[kConvK - 1];
+#pragma unroll
+    for (int j = 0; j < kConvK - 1; ++j)
+        h[j] = slot >= 0 ? ld4v<T>(S + (size_t(slot) * (kConvK - 1) + j) * a.C + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 y;
+    y.x = silu_f(fmaf(r[0].w, xv.x, fmaf(r[0].z, h[2].x, fmaf(r[0].y, h[1].x, fmaf(r[0].x, h[0].x, bias.x)))));
+    y.y = silu_f(fmaf(r[1].w, xv.y, fmaf(r[1].z, h[2].y, fmaf(r[1].y, h[1].y, fmaf(r[1].x, h[0].y, bias.y)))));
+    y.z = silu_f(fmaf(r[2].w, xv.z, fmaf(r[2].z, h[2].z, fmaf(r[2].y, h[1].z, fmaf(r[2].x, h[0].z, bias.z)))));
+    y.w = silu_f(fmaf(r[3].w, xv.w, fmaf(r[3].z, h[2].w, fmaf(r[3].y, h[1].w, fmaf(r[3].x, h[0].w, bias.w)))));
+    const int qk_c = a.hq * kHeadDim;
+    if (a.norm_qk && c0 < 2 * qk_c) {  // uniform over the warp (one head)
+        float ss = y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
+        for (int m = 16; m; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+        const float inv = rsqrtf(ss + 1e-6f);
+        y.x *= inv; y.y *= inv; y.z *= inv; y.w *= inv;
+    }
+    if (c0 < qk_c) st4v<T>(static_cast<T *>(a.oq) + size_t(n) * qk_c + c0, y);
+    else if (c0 < 2 * qk_c) st4v<T>(static_cast<T *>(a.ok) + size_t(n) * qk_c + c0 - qk_c, y);
+    else st4v<T>(static_cast<T *>(a.ov) + size_t(n) * a.hv * kHeadDim + c0 - 2 * qk_c, y);
+    if (slot >= 0) {  // the window moves on by one input
+        st4v<T>(S + (size_t(slot) * (kConvK - 1) + 0) * a.C + c0, h[1]);
+        st4v<T>(S + (size_t(slot) * (kConvK - 1) + 1) * a.C + c0, h[2]);
+        st4v<T>(S + (size_t(slot) * (kConvK - 1) + 2) * a.C + c0, xv);
     }
 }
 
@@ -212,14 +300,38 @@ cudaError_t launch_conv1d_silu(const gdn_problem &p, const void *x, const float 
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    int tile = 1;  // tokens per tile: about two token tiles per SM, 1 .. 64
-    while (tile < 64 && tile * 2 <= p.total_tokens / sms) tile *= 2;
+    // tokens per tile (a power of two, 1 .. 64): the largest that still gives
+    // about four CTAs per SM
+    const int cblocks = (C + kCPerBlock - 1) / kCPerBlock;
+    const int esize = p.io_dtype == GDN_DT_BF16 ? 2 : 4;
+    const int max_tile = kMaxTileBytes / (kCPerBlock * esize);  // 32 (bf16) or 16 (f32)
+    int tile = 1;
+    while (tile < max_tile && int64_t(tile) * 2 * 3 * sms <= int64_t(p.total_tokens) * cblocks) tile *= 2;
+    const size_t smem = size_t(tile + kConvK - 2) * kCPerBlock * esize;  // a tile may grow by two rows
+    const void *fn = p.io_dtype == GDN_DT_BF16 ? reinterpret_cast<const void *>(k_conv1d_silu<__nv_bfloat16>)
+                                               : reinterpret_cast<const void *>(k_conv1d_silu<float>);
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
     ConvArgs a{x, weight, bias, conv_state, state_indices, cu_seqlens, out_q, out_k, out_v,
                p.total_tokens, C, p.num_seqs, p.num_state_slots, p.hq, p.hv, tile, norm_qk, status};
-    const dim3 grid((p.total_tokens + tile - 1) / tile, (C + kCPerBlock - 1) / kCPerBlock);
+    const dim3 grid((p.total_tokens + tile - 1) / tile, cblocks);
     LaunchScope scope(GDN_K_CONV1D_SILU, s);
-    if (p.io_dtype == GDN_DT_BF16) k_conv1d_silu<__nv_bfloat16><<<grid, kCThreads, 0, s>>>(a);
-    else k_conv1d_silu<float><<<grid, kCThreads, 0, s>>>(a);
+    if (p.io_dtype == GDN_DT_BF16) k_conv1d_silu<__nv_bfloat16><<<grid, kCThreads, smem, s>>>(a);
+    else k_conv1d_silu<float><<<grid, kCThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_conv1d_step(const gdn_problem &p, const void *x, const float *weight, const float *bias,
+                               void *conv_state, const int32_t *state_indices, int norm_qk, void *out_q,
+                               void *out_k, void *out_v, int *status, cudaStream_t s) {
+    const int C = (2 * p.hq + p.hv) * kHeadDim;
+    if (p.num_seqs == 0) return cudaSuccess;
+    ConvArgs a{x, weight, bias, conv_state, state_indices, nullptr, out_q, out_k, out_v,
+               p.num_seqs, C, p.num_seqs, p.num_state_slots, p.hq, p.hv, 1, norm_qk, status};
+    const dim3 grid(p.num_seqs, (C + kCPerBlock - 1) / kCPerBlock);
+    LaunchScope scope(GDN_K_CONV1D_STEP, s);
+    if (p.io_dtype == GDN_DT_BF16) k_conv1d_step<__nv_bfloat16><<<grid, kCThreads, 0, s>>>(a);
+    else k_conv1d_step<float><<<grid, kCThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -39,7 +39,7 @@ cudaEvent_t take_event() {
 
 const char *const kNames[GDN_K_COUNT] = {
     "chunk_table", "prep_simt", "state_simt", "output_simt", "recurrent_step",
-    "chunk_fused_tc", "recurrent_step_gated", "gated_rmsnorm", "conv1d_silu", "gating",
+    "chunk_fused_tc", "recurrent_step_gated", "gated_rmsnorm", "conv1d_silu", "gating", "conv1d_step",
 };
 
 }  // namespace

@@ -6,7 +6,8 @@ no fallback: if libgdn.so cannot be built or loaded, ``load()`` raises.
 
 The entry points keep the C names:
   gdn_chunk_fwd, gdn_chunk_fwd_workspace_size, gdn_recurrent_step,
-  gdn_recurrent_step_gated, gdn_gated_rmsnorm, gdn_causal_conv1d_silu, gdn_gating,
+  gdn_recurrent_step_gated, gdn_gated_rmsnorm, gdn_causal_conv1d_silu,
+  gdn_causal_conv1d_silu_step, gdn_gating,
   gdn_read_device_status, gdn_status_string, gdn_version.
 """
 from __future__ import annotations
@@ -26,8 +27,8 @@ GDN_DT_F32, GDN_DT_BF16 = 0, 1
 SYMBOLS = ("gdn_chunk_fwd", "gdn_chunk_fwd_workspace_size", "gdn_recurrent_step", "gdn_read_device_status",
            "gdn_status_string", "gdn_version", "gdn_profile_enable", "gdn_profile_collect", "gdn_kernel_name",
            "gdn_chunk_fwd_noalloc", "gdn_recurrent_step_gated", "gdn_gated_rmsnorm", "gdn_causal_conv1d_silu",
-           "gdn_gating")
-GDN_K_COUNT = 10
+           "gdn_gating", "gdn_causal_conv1d_silu_step")
+GDN_K_COUNT = 11
 
 
 class GdnProblem(ctypes.Structure):
@@ -68,6 +69,9 @@ def load(path: Optional[str] = None):
             lib.gdn_gated_rmsnorm.restype = ctypes.c_int
             lib.gdn_causal_conv1d_silu.argtypes = [P, _vp, _fp, _fp, _vp, _ip, _ip, ctypes.c_int, _vp, _vp, _vp, _vp]
             lib.gdn_causal_conv1d_silu.restype = ctypes.c_int
+            lib.gdn_causal_conv1d_silu_step.argtypes = [P, _vp, _fp, _fp, _vp, _ip, ctypes.c_int, _vp, _vp, _vp,
+                                                        _vp]
+            lib.gdn_causal_conv1d_silu_step.restype = ctypes.c_int
             lib.gdn_gating.argtypes = [P, _fp, _fp, _fp, _fp, _fp, _fp, _vp]
             lib.gdn_gating.restype = ctypes.c_int
             lib.gdn_recurrent_step_gated.restype = ctypes.c_int
@@ -250,6 +254,25 @@ def gdn_causal_conv1d_silu(x, weight, hq, hv, bias=None, conv_state=None, state_
                                        _ptr(v), _stream(stream))
     if st != GDN_OK:
         raise GdnError(st, "gdn_causal_conv1d_silu")
+    return q, k, v
+
+
+def gdn_causal_conv1d_silu_step(x, weight, hq, hv, bias=None, conv_state=None, state_indices=None, norm_qk=False,
+                                q=None, k=None, v=None, stream=None):
+    """gdn_causal_conv1d_silu for one token per sequence: x [N, C]."""
+    N, C = x.shape
+    if C != (2 * hq + hv) * 128:
+        raise ValueError("x must have (2 hq + hv) * 128 channels")
+    slots = 0 if conv_state is None else conv_state.shape[0]
+    prob = GdnProblem(N, 1, N, N, hq, hv, 128, 128, _io_dtype(x), 0, slots)
+    q = torch.empty((N, hq, 128), dtype=x.dtype, device=x.device) if q is None else q
+    k = torch.empty((N, hq, 128), dtype=x.dtype, device=x.device) if k is None else k
+    v = torch.empty((N, hv, 128), dtype=x.dtype, device=x.device) if v is None else v
+    st = load().gdn_causal_conv1d_silu_step(ctypes.byref(prob), _ptr(x), _ptr(weight), _ptr(bias),
+                                            _ptr(conv_state), _ptr(state_indices), int(bool(norm_qk)), _ptr(q),
+                                            _ptr(k), _ptr(v), _stream(stream))
+    if st != GDN_OK:
+        raise GdnError(st, "gdn_causal_conv1d_silu_step")
     return q, k, v
 
 

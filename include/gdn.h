@@ -254,6 +254,14 @@ int gdn_causal_conv1d_silu(const gdn_problem *p, const void *x, const float *wei
                            void *conv_state, const int32_t *state_indices, const int32_t *cu_seqlens,
                            int norm_qk, void *q, void *k, void *v, void *stream);
 
+/* gdn_causal_conv1d_silu for one token per sequence (decode): sequence n is
+ * token n (total_tokens == num_seqs, no offsets); the same arguments
+ * otherwise, with x [num_seqs, C] and q, k, v [num_seqs, h, 128]. Its state
+ * moves on by one input: [s1, s2, x]. */
+int gdn_causal_conv1d_silu_step(const gdn_problem *p, const void *x, const float *weight, const float *bias,
+                                void *conv_state, const int32_t *state_indices, int norm_qk,
+                                void *q, void *k, void *v, void *stream);
+
 /* Gates of every token from the gate projections ([SGL] gdn_gating node;
  * [Kestrel] gating kernel, softplus linear above 20 and exponential below
  * -20): for t < total_tokens, h < hv,
@@ -290,7 +298,8 @@ typedef enum gdn_kernel {
     GDN_K_GATED_RMSNORM = 7,      /* output gate (head-wise RMSNorm, SiLU(z)) over a whole tensor */
     GDN_K_CONV1D_SILU = 8,        /* short causal convolution + SiLU with conv state, split into q, k, v */
     GDN_K_GATING = 9,             /* g and beta from the gate projections, every token */
-    GDN_K_COUNT = 10
+    GDN_K_CONV1D_STEP = 10,       /* short convolution, one token per sequence (decode) */
+    GDN_K_COUNT = 11
 } gdn_kernel;
 
 /* Turns per-kernel CUDA-event timing on (non-zero) or off for every later

@@ -154,3 +154,40 @@ def test_prefill_layer_core_from_projections(cuda, dtype):
     check(y, oracle.gated_rmsnorm(o_r, z, nw, 1e-6), dtype, "y")
     check(S, S_r, dtype, "final state")
     check(st, st_ref, dtype, "conv state")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_conv_step_kernel_chained(cuda, dtype):
+    """gdn_causal_conv1d_silu_step: 256 one-token sequences x 12 steps, q/k
+    norm, a padding slot (-1: zero history, no write), against the oracle."""
+    hq, hv, N = 16, 32, 256
+    _, w, b, st0 = W.make_conv_inputs(69, 1, hq, hv, dtype, slots=N + 1)
+    idx_np = np.random.default_rng(4).permutation(N + 1)[:N].astype(np.int32)
+    idx_np[7] = -1
+    idx = torch.from_numpy(idx_np)
+    cu = torch.arange(N + 1, dtype=torch.int32)
+    st = st0.to(cuda)
+    st_ref = st0.double().numpy()
+    for step in range(12):
+        x, _, _, _ = W.make_conv_inputs(2000 + step, N, hq, hv, dtype)
+        q, k, v = gdn.gdn_causal_conv1d_silu_step(x.to(cuda), w.to(cuda), hq, hv, bias=b.to(cuda), conv_state=st,
+                                                  state_indices=idx.to(cuda), norm_qk=True)
+        torch.cuda.synchronize()
+        y_ref, st_ref = oracle.causal_conv1d_silu(x, w, b, st_ref, cu, idx_np)
+        q_r, k_r, v_r = split_ref(y_ref, hq, hv)
+        if step in (0, 11):
+            check(q, oracle.l2_normalise(q_r), dtype, f"q step {step}")
+            check(k, oracle.l2_normalise(k_r), dtype, f"k step {step}")
+            check(v, v_r, dtype, f"v step {step}")
+    check(st, st_ref, dtype, "conv state after 12 steps")
+
+
+def test_conv_step_out_of_range_slot(cuda):
+    _, w, b, st0 = W.make_conv_inputs(70, 1, 1, 2, torch.float32, slots=2)
+    x, _, _, _ = W.make_conv_inputs(71, 2, 1, 2, torch.float32)
+    st = st0.to(cuda)
+    gdn.gdn_read_device_status(clear=True)
+    gdn.gdn_causal_conv1d_silu_step(x.to(cuda), w.to(cuda), 1, 2, bias=b.to(cuda), conv_state=st,
+                                    state_indices=torch.tensor([1, 5], dtype=torch.int32, device=cuda))
+    assert gdn.gdn_read_device_status(clear=True) == gdn.GDN_EDEVICE_INPUT
+    assert torch.equal(st[0], st0[0].to(cuda))  # slot 0 is nobody's
