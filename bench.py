@@ -10,7 +10,8 @@ flushed by writing a 512 MiB buffer (the inputs, 104 MB, would fit in the
 126 MB L2). Prints ONE JSON line (rank 0). The decode step (256 sequences x 32
 v-heads, f32 state read and written in place) is measured in the same run and
 reported under "decode"; the same step fed raw q/k and gate projections (the
-front-end and the output gate computed in the kernel) under "decode_gated";
+front-end and the output gate computed in the kernel) under "decode_gated",
+and that with a bf16 state cache and bf16 beta under "decode_sglang";
 the stand-alone output gate (gdn_gated_rmsnorm) over the prefill's
 [4096, 32, 128] read-out under "output_gate"; the short convolution (prefill
 projections and one decode step) and the gating under "front_end".
@@ -373,6 +374,8 @@ def run_ours(args, world, rank, local):
 
     decode = None if args.no_decode else run_decode(args, dev, world, peaks, peak_src)
     decode_gated = None if args.no_decode else run_decode(args, dev, world, peaks, peak_src, gated=True)
+    decode_sglang = None if args.no_decode else run_decode(args, dev, world, peaks, peak_src, gated=True,
+                                                           sglang=True)
     output_gate = None if args.no_decode else run_gate_norm(args, dev, world, peaks, peak_src)
     front_end = None if args.no_decode else run_front_end(args, dev, world, peaks, peak_src)
     clocks.stop()
@@ -390,7 +393,8 @@ def run_ours(args, world, rank, local):
                    "chunk": 64, "initial_state": "zero", "final_state": "f32",
                    "l2": L2_NOTE, "parallelism": f"replicas x{world}"},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": gpu_launches,
-        "kernels": kernels, "decode": decode, "decode_gated": decode_gated, "output_gate": output_gate,
+        "kernels": kernels, "decode": decode, "decode_gated": decode_gated, "decode_sglang": decode_sglang,
+        "output_gate": output_gate,
         "front_end": front_end,
         "step_ms": {"median": statistics.median(step_ms), "p10": sorted(step_ms)[len(step_ms) // 10],
                     "p90": sorted(step_ms)[(9 * len(step_ms)) // 10]},
@@ -399,13 +403,16 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
-def run_decode(args, dev, world, peaks, peak_src, gated=False):
+def run_decode(args, dev, world, peaks, peak_src, gated=False, sglang=False):
     """Times the decode step; ``gated`` runs gdn_recurrent_step_gated (raw q/k
-    and gate projections in, front-end in the kernel) instead."""
+    and gate projections in, front-end in the kernel) instead; ``sglang`` adds
+    the packed SGLang kernel's precision (bf16 state cache, bf16 beta)."""
     from gated_deltanet_chunked_gb300 import gdn
 
     w = DECODE
     state = W.make_decode_state(w).to(dev)
+    if sglang:
+        state = state.to(torch.bfloat16)
     make = W.make_decode_step_gated if gated else W.make_decode_step
     sets = []
     for s in range(4):
@@ -419,7 +426,7 @@ def run_decode(args, dev, world, peaks, peak_src, gated=False):
         x = sets[i % len(sets)]
         if gated:
             gdn.gdn_recurrent_step_gated(x["q"], x["k"], x["v"], x["a"], x["b"], A_log, dt_bias, x["scale"],
-                                         state, out=out, z=z, norm_weight=norm_w, norm_eps=1e-6)
+                                         state, out=out, z=z, norm_weight=norm_w, norm_eps=1e-6, beta_bf16=sglang)
         else:
             gdn.gdn_recurrent_step(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], state, out=out)
 
@@ -442,7 +449,7 @@ def run_decode(args, dev, world, peaks, peak_src, gated=False):
     prof = gdn.gdn_profile_collect(reset=True)
     ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(e0, e1)) / steps, world, dev)
     n_pairs = w.num_seqs * w.hv
-    state_bytes = 2 * n_pairs * 128 * 128 * 4
+    state_bytes = 2 * n_pairs * 128 * 128 * state.element_size()
     # q, k, v, out in bf16; g, beta (or a, b) f32 per (sequence, v-head); A_log, dt_bias f32 per v-head
     # gated: + z (bf16, like v) per (sequence, v-head) and the 128-float norm weight
     io_bytes = w.num_seqs * (w.hq * 128 * 2 * 2 + w.hv * 128 * 2 * 2 + w.hv * 8)
@@ -456,12 +463,13 @@ def run_decode(args, dev, world, peaks, peak_src, gated=False):
         "workload": w.name, "steps": steps, "ms_per_step": ms, "value": world * total / (ms * 1e-3) / 1e9,
         "unit": "GB/s", "state_bytes_per_step": state_bytes, "bytes_per_step": total,
         "inputs": ("raw q/k, gate projections a/b, A_log/dt_bias, output gate z + RMSNorm weight "
-                   "(front-end and output gate in the kernel)" if gated else "normalised q/k, g, beta"),
+                   "(front-end and output gate in the kernel)" if gated else "normalised q/k, g, beta")
+                  + ("; bf16 state cache, bf16 beta" if sglang else "; f32 state"),
         "roofline": {"kernel": kname, "bound": "hbm", "achieved": total / (k_ms * 1e-3) / 1e9,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": total / (k_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "traffic": ncu_traffic(kname),
                      "peak_source": f"{peak_src} (hbm_gbs, burst copy)"},
-        "l2": "state (537 MB) larger than L2; no flush",
+        "l2": f"state ({state.numel() * state.element_size() / 1e6:.0f} MB) larger than L2; no flush",
     }
 
 

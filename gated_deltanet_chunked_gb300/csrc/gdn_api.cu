@@ -36,14 +36,15 @@ inline bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Checks shared by prefill and decode. Returns GDN_OK or the error code.
-int check_common(const gdn_problem *p) {
+// `allowed_flags`: the gdn_problem.flags bits the entry point accepts.
+int check_common(const gdn_problem *p, uint32_t allowed_flags = 0) {
     if (!p) return GDN_EINVAL;
     if (p->hq <= 0 || p->hv <= 0 || p->dk <= 0 || p->dv <= 0) return GDN_EINVAL;
     if (p->hv % p->hq != 0) return GDN_EINVAL;
     if (p->io_dtype != GDN_DT_F32 && p->io_dtype != GDN_DT_BF16) return GDN_EINVAL;
     if (p->num_seqs < 0 || p->total_tokens < 0) return GDN_EINVAL;
     if (p->dk != kHeadDim || p->dv != kHeadDim) return GDN_EUNSUPPORTED;
-    if (p->flags != 0) return GDN_EUNSUPPORTED;
+    if (p->flags & ~allowed_flags) return GDN_EUNSUPPORTED;
     return GDN_OK;
 }
 
@@ -154,10 +155,12 @@ int gdn_chunk_fwd(const gdn_problem *p, const void *q, const void *k, const void
     return cuda_status(launch_prefill_simt(a, ws + L.data_off, s));
 }
 
+constexpr uint32_t kDecodeFlags = GDN_FLAG_BETA_BF16 | GDN_FLAG_STATE_BF16;
+
 int gdn_recurrent_step(const gdn_problem *p, const void *q, const void *k, const void *v, const float *g,
-                       const float *beta, float scale, float *state, const int32_t *state_indices, void *out,
+                       const float *beta, float scale, void *state, const int32_t *state_indices, void *out,
                        void *stream) {
-    int st = check_common(p);
+    int st = check_common(p, kDecodeFlags);
     if (st) return st;
     if (p->total_tokens != p->num_seqs) return GDN_EINVAL;
     if (p->num_state_slots < 0 || (!state_indices && p->num_state_slots < p->num_seqs)) return GDN_EINVAL;
@@ -175,10 +178,10 @@ int gdn_recurrent_step(const gdn_problem *p, const void *q, const void *k, const
 }
 
 int gdn_recurrent_step_gated(const gdn_problem *p, const void *q, const void *k, const void *v, const float *a,
-                             const float *b, const float *A_log, const float *dt_bias, float scale, float *state,
+                             const float *b, const float *A_log, const float *dt_bias, float scale, void *state,
                              const int32_t *state_indices, const void *z, const float *norm_weight,
                              float norm_eps, void *out, void *stream) {
-    int st = check_common(p);
+    int st = check_common(p, kDecodeFlags);
     if (st) return st;
     if (p->total_tokens != p->num_seqs) return GDN_EINVAL;
     if (p->num_state_slots < 0 || (!state_indices && p->num_state_slots < p->num_seqs)) return GDN_EINVAL;

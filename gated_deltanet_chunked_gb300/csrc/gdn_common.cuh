@@ -133,7 +133,7 @@ __device__ __forceinline__ float silu_f(float x) {
 // L2-normalised in the kernel.
 cudaError_t launch_recurrent_step(const gdn_problem &p, const void *q, const void *k, const void *v,
                                   const float *g, const float *beta, const DecodeFront *front, float scale,
-                                  float *state, const int32_t *state_indices, void *out, int *status,
+                                  void *state, const int32_t *state_indices, void *out, int *status,
                                   cudaStream_t s);
 
 }  // namespace gdn

@@ -31,6 +31,9 @@
 //   d' = rk beta (v - alpha rk p),  S' = alpha S_old + k^T d',
 //   o  = scale rq (alpha r + qk d')
 // with p, r, qk the raw-row reductions above. The state traffic is unchanged.
+// The SGLang parity options of that page: a bf16 state cache (loaded to f32,
+// written back rounded to bf16: half the traffic) and beta rounded to bf16
+// before use.
 // With an output gate z (the sgl-qwen3-5-moe page's output_rmsnorm_silu_gate,
 // norm before gate), warp 0, which holds the head's 128 outputs, finishes
 //   y = o / sqrt(mean(o^2) + eps) * weight * silu(z)
@@ -77,12 +80,33 @@ __device__ __forceinline__ float4 ld4<__nv_bfloat16>(const void *p, size_t i) {
     return make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 
-template <typename T, bool kFront, bool kGateOut>
-__global__ void __launch_bounds__(kRThreads, 2)
+// state words as loaded: float4 (f32 cache) or 4 packed bf16 (bf16 cache,
+// widened where used, so that the registers hold twice the rows in flight)
+template <typename ST>
+struct StateWords;
+template <>
+struct StateWords<float> {
+    using raw = float4;
+    static __device__ __forceinline__ raw load(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+    static __device__ __forceinline__ float4 f(const raw &r) { return r; }
+};
+template <>
+struct StateWords<__nv_bfloat16> {
+    using raw = uint2;
+    static __device__ __forceinline__ raw load(const __nv_bfloat16 *p) { return *reinterpret_cast<const uint2 *>(p); }
+    static __device__ __forceinline__ float4 f(const raw &r) {
+        const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.x));
+        const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&r.y));
+        return make_float4(lo.x, lo.y, hi.x, hi.y);
+    }
+};
+
+template <typename T, typename ST, bool kFront, bool kGateOut>
+__global__ void __launch_bounds__(kRThreads, sizeof(ST) == 2 ? 3 : 2)
 k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const void *__restrict__ v,
                  const float *__restrict__ g, const float *__restrict__ beta, DecodeFront front, float scale,
-                 float *__restrict__ state, const int32_t *__restrict__ idx, void *__restrict__ out,
-                 int num_seqs, int hq, int hv, int slots, int *status) {
+                 void *__restrict__ state, const int32_t *__restrict__ idx, void *__restrict__ out,
+                 int num_seqs, int hq, int hv, int slots, int beta_bf16, int *status) {
     __shared__ float ks[kHeadDim], qs[kHeadDim];
     __shared__ float4 red_p[kRThreads / 32][32], red_r[kRThreads / 32][32];
     __shared__ float qk_s, rk_s, rq_s, alpha_s, beta_s;
@@ -96,7 +120,7 @@ k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const v
         if (tid == 0) record_status(status, GDN_EDEVICE_INPUT);
         return;
     }
-    float4 *S = reinterpret_cast<float4 *>(state + (size_t(slot) * hv + h) * kHeadDim * kHeadDim);
+    ST *S = static_cast<ST *>(state) + (size_t(slot) * hv + h) * kHeadDim * kHeadDim;
     // The small inputs are issued first, each by the warp that uses it, so that
     // they arrive while the 64 KiB state read is still in flight. Nothing but
     // the q/k staging stands before the first barrier: the front-end's scalar
@@ -128,9 +152,9 @@ k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const v
         kq_q = ldx<T>(q, qk_off);
     }
     // all state loads: 16 independent 128-bit loads per thread
-    float4 s[kRowsPerThread];
+    typename StateWords<ST>::raw s[kRowsPerThread];
 #pragma unroll
-    for (int i = 0; i < kRowsPerThread; ++i) s[i] = S[(wrow + 8 * i) * 32 + lane];
+    for (int i = 0; i < kRowsPerThread; ++i) s[i] = StateWords<ST>::load(S + size_t(wrow + 8 * i) * kHeadDim + 4 * lane);
     if (tid < kHeadDim) {
         ks[tid] = kq_k;
         qs[tid] = kq_q;
@@ -159,10 +183,11 @@ k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const v
 #pragma unroll
     for (int i = 0; i < kRowsPerThread; ++i) {
         const float kd = ks[wrow + 8 * i], qd = qs[wrow + 8 * i];
-        p.x = fmaf(kd, s[i].x, p.x); p.y = fmaf(kd, s[i].y, p.y);
-        p.z = fmaf(kd, s[i].z, p.z); p.w = fmaf(kd, s[i].w, p.w);
-        r.x = fmaf(qd, s[i].x, r.x); r.y = fmaf(qd, s[i].y, r.y);
-        r.z = fmaf(qd, s[i].z, r.z); r.w = fmaf(qd, s[i].w, r.w);
+        const float4 si = StateWords<ST>::f(s[i]);
+        p.x = fmaf(kd, si.x, p.x); p.y = fmaf(kd, si.y, p.y);
+        p.z = fmaf(kd, si.z, p.z); p.w = fmaf(kd, si.w, p.w);
+        r.x = fmaf(qd, si.x, r.x); r.y = fmaf(qd, si.y, r.y);
+        r.z = fmaf(qd, si.z, r.z); r.w = fmaf(qd, si.w, r.w);
     }
     red_p[wrow][lane] = p;
     red_r[wrow][lane] = r;
@@ -183,6 +208,7 @@ k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const v
         alpha = expf(ga);
         b = gb;
     }
+    if (beta_bf16) b = __bfloat162float(__float2bfloat16_rn(b));  // the packed SGLang kernel's rounding
     float rk = 1.f, oscale = scale;
     if (kFront) {
         rk = rk_s;
@@ -217,34 +243,45 @@ k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const v
 #pragma unroll
     for (int i = 0; i < kRowsPerThread; ++i) {
         const float kd = ks[wrow + 8 * i];
+        const float4 si = StateWords<ST>::f(s[i]);
         float4 t;
-        t.x = fmaf(alpha, s[i].x, kd * d.x);
-        t.y = fmaf(alpha, s[i].y, kd * d.y);
-        t.z = fmaf(alpha, s[i].z, kd * d.z);
-        t.w = fmaf(alpha, s[i].w, kd * d.w);
-        S[(wrow + 8 * i) * 32 + lane] = t;
+        t.x = fmaf(alpha, si.x, kd * d.x);
+        t.y = fmaf(alpha, si.y, kd * d.y);
+        t.z = fmaf(alpha, si.z, kd * d.z);
+        t.w = fmaf(alpha, si.w, kd * d.w);
+        st4<ST>(S, size_t(wrow + 8 * i) * kHeadDim + 4 * lane, t);
     }
 }
 
 }  // namespace
 
+namespace {
+using StepKernel = void (*)(const void *, const void *, const void *, const float *, const float *, DecodeFront,
+                            float, void *, const int32_t *, void *, int, int, int, int, int, int *);
+
+template <typename T, typename ST>
+StepKernel pick_step(bool front, bool gate) {
+    return gate ? k_recurrent_step<T, ST, true, true>
+                : front ? k_recurrent_step<T, ST, true, false> : k_recurrent_step<T, ST, false, false>;
+}
+}  // namespace
+
 cudaError_t launch_recurrent_step(const gdn_problem &p, const void *q, const void *k, const void *v,
                                   const float *g, const float *beta, const DecodeFront *front, float scale,
-                                  float *state, const int32_t *state_indices, void *out, int *status,
+                                  void *state, const int32_t *state_indices, void *out, int *status,
                                   cudaStream_t s) {
     const unsigned pairs = unsigned(p.num_seqs) * unsigned(p.hv);
     if (pairs == 0) return cudaSuccess;
     LaunchScope scope(front ? GDN_K_RECURRENT_STEP_GATED : GDN_K_RECURRENT_STEP, s);
     const DecodeFront f = front ? *front : DecodeFront{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, 0.f};
     const bool gate = front && front->z;
-    auto kern = p.io_dtype == GDN_DT_BF16
-                    ? (gate ? k_recurrent_step<__nv_bfloat16, true, true>
-                            : front ? k_recurrent_step<__nv_bfloat16, true, false>
-                                    : k_recurrent_step<__nv_bfloat16, false, false>)
-                    : (gate ? k_recurrent_step<float, true, true>
-                            : front ? k_recurrent_step<float, true, false> : k_recurrent_step<float, false, false>);
+    const bool st_bf = (p.flags & GDN_FLAG_STATE_BF16) != 0;
+    const StepKernel kern =
+        p.io_dtype == GDN_DT_BF16
+            ? (st_bf ? pick_step<__nv_bfloat16, __nv_bfloat16>(front, gate) : pick_step<__nv_bfloat16, float>(front, gate))
+            : (st_bf ? pick_step<float, __nv_bfloat16>(front, gate) : pick_step<float, float>(front, gate));
     kern<<<pairs, kRThreads, 0, s>>>(q, k, v, g, beta, f, scale, state, state_indices, out, p.num_seqs, p.hq,
-                                    p.hv, p.num_state_slots, status);
+                                    p.hv, p.num_state_slots, (p.flags & GDN_FLAG_BETA_BF16) ? 1 : 0, status);
     return cudaGetLastError();
 }
 

@@ -23,6 +23,7 @@ from . import build as _build
 GDN_OK, GDN_EINVAL, GDN_EUNSUPPORTED, GDN_ECUDA, GDN_ETIMEOUT, GDN_EDEVICE_INPUT, GDN_ETOOBIG = range(7)
 GDN_NOALLOC_SCRATCH_BYTES = 32 << 20
 GDN_DT_F32, GDN_DT_BF16 = 0, 1
+GDN_FLAG_BETA_BF16, GDN_FLAG_STATE_BF16 = 1 << 1, 1 << 2
 
 SYMBOLS = ("gdn_chunk_fwd", "gdn_chunk_fwd_workspace_size", "gdn_recurrent_step", "gdn_read_device_status",
            "gdn_status_string", "gdn_version", "gdn_profile_enable", "gdn_profile_collect", "gdn_kernel_name",
@@ -187,10 +188,17 @@ def gdn_chunk_fwd_noalloc(q, k, v, g, beta, scale, out, final_state=None, initia
     return out, final_state
 
 
-def gdn_recurrent_step(q, k, v, g, beta, scale, state, state_indices=None, out=None, stream=None):
-    """One decode step; ``state`` [slots, Hv, 128, 128] f32 is updated in place."""
+def _decode_flags(state, beta_bf16):
+    return (GDN_FLAG_STATE_BF16 if state.dtype == torch.bfloat16 else 0) | (GDN_FLAG_BETA_BF16 if beta_bf16 else 0)
+
+
+def gdn_recurrent_step(q, k, v, g, beta, scale, state, state_indices=None, out=None, stream=None,
+                       beta_bf16=False):
+    """One decode step; ``state`` [slots, Hv, 128, 128] (f32, or bf16 for a
+    bf16 state cache) is updated in place. ``beta_bf16`` rounds beta to bf16."""
     N, hq, dk = q.shape
-    prob = GdnProblem(N, 1, N, N, hq, v.shape[1], dk, v.shape[2], _io_dtype(q), 0, state.shape[0])
+    prob = GdnProblem(N, 1, N, N, hq, v.shape[1], dk, v.shape[2], _io_dtype(q), _decode_flags(state, beta_bf16),
+                      state.shape[0])
     if out is None:
         out = torch.empty(v.shape, dtype=v.dtype, device=v.device)
     st = load().gdn_recurrent_step(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
@@ -202,13 +210,15 @@ def gdn_recurrent_step(q, k, v, g, beta, scale, state, state_indices=None, out=N
 
 
 def gdn_recurrent_step_gated(q, k, v, a, b, A_log, dt_bias, scale, state, state_indices=None, out=None,
-                             stream=None, z=None, norm_weight=None, norm_eps=1e-6):
+                             stream=None, z=None, norm_weight=None, norm_eps=1e-6, beta_bf16=False):
     """Decode step from raw q/k and the gate projections a, b [N, Hv] with
     per-head A_log, dt_bias [Hv] (all f32); ``state`` is updated in place.
     With ``z`` [N, Hv, 128] and ``norm_weight`` [128] f32 the output gate
-    (head-wise RMSNorm, then silu(z)) is applied before the store."""
+    (head-wise RMSNorm, then silu(z)) is applied before the store. A bf16
+    ``state`` is a bf16 state cache; ``beta_bf16`` rounds beta to bf16."""
     N, hq, dk = q.shape
-    prob = GdnProblem(N, 1, N, N, hq, v.shape[1], dk, v.shape[2], _io_dtype(q), 0, state.shape[0])
+    prob = GdnProblem(N, 1, N, N, hq, v.shape[1], dk, v.shape[2], _io_dtype(q), _decode_flags(state, beta_bf16),
+                      state.shape[0])
     if out is None:
         out = torch.empty(v.shape, dtype=v.dtype, device=v.device)
     st = load().gdn_recurrent_step_gated(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b),

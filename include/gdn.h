@@ -73,6 +73,12 @@ typedef enum gdn_dtype {
     GDN_DT_BF16 = 1
 } gdn_dtype;
 
+/* gdn_problem.flags: options of the decode entry points, the precision of
+ * [SGL]'s packed decode kernel (node 7). Prefill entry points want 0. */
+#define GDN_FLAG_BETA_BF16 (1u << 1)  /* beta rounded to the nearest bf16 (ties to even) before use */
+#define GDN_FLAG_STATE_BF16 (1u << 2) /* the state array holds bf16: loaded to f32, the updated state
+                                          rounded to bf16 when written back */
+
 /* Problem descriptor.
  *  Dense prefill  : batch = B, seqlen = T, num_seqs = B, total_tokens = B*T,
  *                   cu_seqlens = NULL (sequence b = rows [b*T, (b+1)*T)).
@@ -91,7 +97,7 @@ typedef struct gdn_problem {
     int32_t dk;
     int32_t dv;
     int32_t io_dtype;         /* gdn_dtype of q, k, v and out */
-    uint32_t flags;           /* reserved, must be 0 */
+    uint32_t flags;           /* GDN_FLAG_* bits (decode only); 0 for prefill */
     int32_t num_state_slots;  /* decode only */
 } gdn_problem;
 
@@ -159,14 +165,17 @@ int gdn_chunk_fwd_noalloc(const gdn_problem *p, const void *q, const void *k, co
  *   S = alpha * state[s,h];  p = k_n S;  d = beta (v_n - p);
  *   state[s,h] = S + k_n^T d;  out[n,h] = scale * q_n state[s,h].
  *   q, k [num_seqs, hq, 128]; v, out [num_seqs, hv, 128]; g, beta [num_seqs, hv]
- *   state [num_state_slots, hv, 128, 128] f32, read and written in place.
+ *   state [num_state_slots, hv, 128, 128] f32 (bf16 with GDN_FLAG_STATE_BF16),
+ *   read and written in place; arithmetic is f32 either way.
+ *   p->flags may hold GDN_FLAG_BETA_BF16 and GDN_FLAG_STATE_BF16 (any other
+ *   bit: GDN_EUNSUPPORTED).
  *   state_indices int32 [num_seqs] or NULL. A negative index skips the
  *   sequence (its out rows are not written: a padding slot). An index
  *   >= num_state_slots is skipped and recorded as GDN_EDEVICE_INPUT.
  *   Two sequences must not name the same slot (their updates would race). */
 int gdn_recurrent_step(const gdn_problem *p, const void *q, const void *k, const void *v,
                        const float *g, const float *beta, float scale,
-                       float *state, const int32_t *state_indices,
+                       void *state, const int32_t *state_indices,
                        void *out, void *stream);
 
 /* Decode step from the raw projections: gdn_recurrent_step with its
@@ -187,7 +196,7 @@ int gdn_recurrent_step(const gdn_problem *p, const void *q, const void *k, const
  *             b the write strength)
  *   A_log, dt_bias [hv] f32: per-head parameters
  *   scale     the query scale, 1/sqrt(128) on the pages; applied once
- *   state, state_indices: as gdn_recurrent_step (f32, in place; negative
+ *   state, state_indices, flags: as gdn_recurrent_step (in place; negative
  *             index = padding slot, skipped; index >= num_state_slots is
  *             skipped and recorded as GDN_EDEVICE_INPUT).
  * All pointers are caller-owned device memory; q, k, v, out, state and
@@ -200,10 +209,11 @@ int gdn_recurrent_step(const gdn_problem *p, const void *q, const void *k, const
  *             without rounding o first); with z NULL out receives o and
  *             norm_weight is ignored.
  * Returns GDN_EINVAL (nothing launched) on a bad descriptor or pointer.
- * beta is used in f32, without the bf16 rounding of [SGL]'s packed kernel. */
+ * beta is used in f32 unless p->flags holds GDN_FLAG_BETA_BF16 (the bf16
+ * rounding of [SGL]'s packed kernel). */
 int gdn_recurrent_step_gated(const gdn_problem *p, const void *q, const void *k, const void *v,
                              const float *a, const float *b, const float *A_log, const float *dt_bias,
-                             float scale, float *state, const int32_t *state_indices,
+                             float scale, void *state, const int32_t *state_indices,
                              const void *z, const float *norm_weight, float norm_eps,
                              void *out, void *stream);
 

@@ -155,14 +155,26 @@ def chunked(q, k, v, g, beta, scale, initial_state=None, cu_seqlens=None, chunk_
     return _finish(out, fin, sh)
 
 
-def recurrent_step(q, k, v, g, beta, scale, state, state_indices=None):
+def recurrent_step(q, k, v, g, beta, scale, state, state_indices=None, beta_bf16=False, state_bf16=False):
     """One decode step for N sequences, each with one token.
 
     q, k: [N, Hq, dk]; v: [N, Hv, dv]; g, beta: [N, Hv]; state: [slots, Hv, dk, dv].
     Sequence n reads and writes slot ``state_indices[n]`` (identity when None);
     a negative index skips the sequence (its output row stays zero). Returns
     (o [N, Hv, dv], new_state [slots, Hv, dk, dv]) without touching ``state``.
+    The precision options of the packed SGLang decode kernel: ``beta_bf16``
+    rounds beta to the nearest bf16 first; ``state_bf16`` rounds the updated
+    slots to the nearest bf16 (a bf16 state cache).
     """
+    if beta_bf16:
+        beta = round_to_bf16(_f64(beta))
+    out, st = _recurrent_step_f64(q, k, v, g, beta, scale, state, state_indices)
+    if state_bf16:
+        st = round_to_bf16(st)
+    return out, st
+
+
+def _recurrent_step_f64(q, k, v, g, beta, scale, state, state_indices):
     st = _f64(state).copy()
     N = int(_f64(q).shape[0])
     idx = np.arange(N) if state_indices is None else np.asarray(
@@ -234,21 +246,20 @@ def l2_normalise(x, eps=QK_NORM_EPS):
 
 
 def recurrent_step_gated(q, k, v, a, b, A_log, dt_bias, scale, state, state_indices=None,
-                         beta_bf16=False):
+                         beta_bf16=False, state_bf16=False):
     """One decode step from raw projections, in the order of decode node 7.
 
     q, k: [N, Hq, dk] raw (not normalised); v: [N, Hv, dv]; a, b: [N, Hv];
     A_log, dt_bias: [Hv]; ``scale`` is the query scale (1/sqrt(d_k) on the
     pages), applied once, to q_bar. With ``beta_bf16`` the write strength is
     rounded to the nearest bf16 (ties to even) before use. Everything else as
-    ``recurrent_step``; returns (o, new_state).
+    ``recurrent_step`` (``state_bf16`` included); returns (o, new_state).
     """
     k_bar = l2_normalise(k)
     q_bar = float(scale) * l2_normalise(q)
     g, beta = decode_gates(a, b, A_log, dt_bias)
-    if beta_bf16:
-        beta = round_to_bf16(beta)
-    return recurrent_step(q_bar, k_bar, v, g, beta, 1.0, state, state_indices)
+    return recurrent_step(q_bar, k_bar, v, g, beta, 1.0, state, state_indices, beta_bf16=beta_bf16,
+                          state_bf16=state_bf16)
 
 
 def round_to_bf16(x):

@@ -107,6 +107,7 @@ def test_recurrent_step_rejects_bad_problems():
     assert step(problem(**{**ok, "num_state_slots": 3})) == gdn.GDN_EINVAL  # identity map needs N slots
     assert step(problem(**{**ok, "total_tokens": 5})) == gdn.GDN_EINVAL
     assert step(problem(**{**ok, "dk": 96})) == gdn.GDN_EUNSUPPORTED
+    assert step(problem(**{**ok, "flags": 16})) == gdn.GDN_EUNSUPPORTED
     assert step(problem(**ok), ptr=FAKE + 2) == gdn.GDN_EINVAL
     assert step(problem(**ok), idx=FAKE + 4) == gdn.GDN_EINVAL
 
@@ -125,7 +126,8 @@ def test_recurrent_step_gated_rejects_bad_problems():
     assert step(problem(**{**ok, "num_state_slots": 3})) == gdn.GDN_EINVAL
     assert step(problem(**{**ok, "total_tokens": 5})) == gdn.GDN_EINVAL
     assert step(problem(**{**ok, "dv": 64})) == gdn.GDN_EUNSUPPORTED
-    assert step(problem(**{**ok, "flags": 2})) == gdn.GDN_EUNSUPPORTED
+    assert step(problem(**{**ok, "flags": 1})) == gdn.GDN_EUNSUPPORTED  # bit 0 is no decode option
+    assert step(problem(**{**ok, "flags": 8})) == gdn.GDN_EUNSUPPORTED
     assert step(problem(**ok), ptr=FAKE + 4) == gdn.GDN_EINVAL  # tensors want 16-byte alignment
     assert step(problem(**ok), gate=FAKE + 2) == gdn.GDN_EINVAL  # gate inputs want 4-byte alignment
     assert step(problem(**ok), b=0) == gdn.GDN_EINVAL

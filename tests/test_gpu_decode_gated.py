@@ -171,3 +171,44 @@ def test_gated_decode_full_with_output_gate(cuda):
     o_ref, st_ref = step_ref(inp, A_log, dt_bias, state0)
     check(y, oracle.gated_rmsnorm(o_ref, z, weight, 1e-6), torch.bfloat16, "y")
     check(state, st_ref, torch.bfloat16, "state")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+@pytest.mark.parametrize("gated", [False, True], ids=["plain", "gated"])
+def test_sglang_precision_mode(cuda, dtype, gated):
+    """bf16 state cache + bf16 beta, 30 chained steps with padding slots,
+    against the oracle with the same two roundings. With a bf16 state the
+    comparison is normwise whatever the io dtype (the state itself carries
+    bf16 rounding; a 1-ulp tie difference between the f32 kernel and the f64
+    oracle is 0.4% of that element)."""
+    w = W.Workload("sgl", 72, "decode", dtype, hq=2, hv=4, num_seqs=6, s0_sigma=0.05)
+    A_log, dt_bias = W.make_decode_gate_params(w)
+    rng = np.random.default_rng(7)
+    state0 = torch.from_numpy(rng.standard_normal((8, 4, 128, 128)).astype(np.float32) * 0.05).to(torch.bfloat16)
+    idx = torch.tensor([5, -1, 0, 7, 2, -1], dtype=torch.int32)
+    state = state0.to(cuda)
+    st_ref = state0.double().numpy()
+    for step in range(30):
+        if gated:
+            inp = W.make_decode_step_gated(w, step)
+            d = to_dev(inp, cuda)
+            o = gdn.gdn_recurrent_step_gated(d["q"], d["k"], d["v"], d["a"], d["b"], A_log.to(cuda),
+                                             dt_bias.to(cuda), d["scale"], state, state_indices=idx.to(cuda),
+                                             beta_bf16=True)
+            o_ref, st_ref = oracle.recurrent_step_gated(inp["q"], inp["k"], inp["v"], inp["a"], inp["b"], A_log,
+                                                        dt_bias, inp["scale"], st_ref, idx.numpy(), beta_bf16=True,
+                                                        state_bf16=True)
+        else:
+            inp = W.make_decode_step(w, step)
+            d = to_dev(inp, cuda)
+            o = gdn.gdn_recurrent_step(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], state,
+                                       state_indices=idx.to(cuda), beta_bf16=True)
+            o_ref, st_ref = oracle.recurrent_step(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["scale"],
+                                                  st_ref, idx.numpy(), beta_bf16=True, state_bf16=True)
+        torch.cuda.synchronize()
+        live = [0, 2, 3, 4]
+        if step in (0, 29):
+            check(o[live], o_ref[live], torch.bfloat16, f"o step {step}")
+    assert gdn.gdn_read_device_status() == gdn.GDN_OK
+    check(state, st_ref, torch.bfloat16, "bf16 state after 30 steps")
+    assert torch.equal(state[[1, 3, 4, 6]], state0[[1, 3, 4, 6]].to(cuda))  # nobody's slots

@@ -555,3 +555,18 @@ def test_conv_constant_input():
     out, _ = oracle.causal_conv1d_silu(np.full((7, 2), 3.0), w, b)
     np.testing.assert_allclose(out[3:, 0], _silu1(3.0 * 1.0 + 0.5), rtol=1e-14)
     np.testing.assert_allclose(out[3:, 1], _silu1(-0.5), rtol=1e-14)
+
+
+def test_decode_precision_options():
+    """bf16 beta and a bf16 state cache: the plain step on rounded beta, its
+    updated slots rounded (both through the pinned bf16 rounding), other slots
+    untouched."""
+    q, k, v, g, beta, _, _ = rand_inputs(71, [3], 1, 2, 8, 8)
+    state = oracle.round_to_bf16(np.random.default_rng(2).standard_normal((5, 2, 8, 8)))
+    idx = np.array([4, -1, 1])
+    o, st = oracle.recurrent_step(q, k, v, g, beta, 0.5, state, idx, beta_bf16=True, state_bf16=True)
+    o2, st2 = oracle.recurrent_step(q, k, v, g, oracle.round_to_bf16(beta), 0.5, state, idx)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(st, oracle.round_to_bf16(st2))
+    np.testing.assert_array_equal(st[[0, 2, 3]], state[[0, 2, 3]])
+    assert np.all(oracle.round_to_bf16(st) == st)
