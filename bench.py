@@ -467,7 +467,8 @@ def run_decode(args, dev, world, peaks, peak_src, gated=False, sglang=False):
                   + ("; bf16 state cache, bf16 beta" if sglang else "; f32 state"),
         "roofline": {"kernel": kname, "bound": "hbm", "achieved": total / (k_ms * 1e-3) / 1e9,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": total / (k_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], "traffic": ncu_traffic(kname),
+                     "frac": total / (k_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                     "traffic": ncu_traffic(kname + ("_bf16state" if sglang else "")),
                      "peak_source": f"{peak_src} (hbm_gbs, burst copy)"},
         "l2": f"state ({state.numel() * state.element_size() / 1e6:.0f} MB) larger than L2; no flush",
     }
@@ -563,7 +564,8 @@ def run_front_end(args, dev, world, peaks, peak_src):
         res[name] = {"ms_per_launch": k_ms, "bytes_per_launch": total,
                      "roofline": {"kernel": kname, "bound": "hbm", "achieved": total / (k_ms * 1e-3) / 1e9,
                                   "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                  "frac": total / (k_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+                                  "frac": total / (k_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                                  "traffic": ncu_traffic(kname)},
                      "l2": f"inputs rotate over {nsets} sets; no flush"}
         del sets
     # gating of every token of the prefill workload ([4096, 32] a, b in; g, beta out)
