@@ -10,14 +10,14 @@
 //
 // HBM-bound: per (token, head) row it reads o and z and writes y
 // (3 x 128 elements). Rows are contiguous, so a block of rows of o (and of z)
-// is one linear range: each CTA streams blocks of 16 KiB per tensor into
-// shared memory with bulk copies (cp.async.bulk, completing on an mbarrier),
-// kStages blocks deep, from one producer thread, while eight consumer warps
-// take four rows at a time (4 channels per lane; four independent chains, as
+// is one linear range: each CTA streams blocks of kBlockRows rows per tensor
+// into shared memory with bulk copies (cp.async.bulk, completing on an
+// mbarrier), kStages blocks deep, from one producer thread, while eight
+// consumer warps take four rows at a time (4 channels per lane; four independent chains, as
 // the kernel is otherwise bound by the latency of its reductions), reduce each
 // row's sum of squares with shuffles and store y straight to global memory
-// (fully coalesced, one 8- or 16-byte store per lane). The grid is two CTAs per SM; CTA b takes
-// blocks b, b + grid, ...
+// (fully coalesced, one 8- or 16-byte store per lane). The grid is kCtasPerSm
+// CTAs per SM; CTA b takes blocks b, b + grid, ...
 #include "gdn_common.cuh"
 #include "tc_ptx.cuh"
 
@@ -27,8 +27,14 @@ namespace {
 constexpr int kConsumerWarps = 8;
 constexpr int kNThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
 constexpr int kStages = 3;
-constexpr uint32_t kBlockBytes = 16384;  // per tensor and stage
-constexpr size_t kSmemBytes = size_t(2) * kStages * kBlockBytes + 1024;
+constexpr int kBlockRows = 64;  // rows per block, a multiple of 4 x kConsumerWarps (32 .. 64 measured alike)
+constexpr int kCtasPerSm = 2;
+
+// bytes of one block of one tensor
+template <typename T>
+__host__ __device__ constexpr uint32_t block_bytes() { return uint32_t(kBlockRows) * kHeadDim * sizeof(T); }
+template <typename T>
+__host__ __device__ constexpr size_t smem_bytes() { return size_t(2) * kStages * block_bytes<T>() + 128; }
 
 template <typename T>
 struct Vec4;
@@ -53,14 +59,15 @@ struct Vec4<__nv_bfloat16> {
 };
 
 template <typename T>
-__global__ void __launch_bounds__(kNThreads, 2)
+__global__ void __launch_bounds__(kNThreads, kCtasPerSm)
 k_gated_rmsnorm(const void *__restrict__ o, const void *__restrict__ z, const float *__restrict__ weight,
                 float eps, void *y, long long rows, int *status) {
     using namespace tc;
     using V = typename Vec4<T>::type;
     constexpr uint32_t kRowBytes = kHeadDim * sizeof(T);
-    constexpr int kRows = int(kBlockBytes / kRowBytes);  // rows per block: 64 (bf16) or 32 (f32)
-    constexpr int kRowsPerWarp = kRows / kConsumerWarps;  // 8 or 4
+    constexpr int kRows = kBlockRows;
+    constexpr uint32_t kBlockBytes = block_bytes<T>();
+    constexpr int kRowsPerWarp = kRows / kConsumerWarps;
     static_assert(kRowsPerWarp % 4 == 0, "rows are taken four at a time");
     extern __shared__ __align__(128) uint8_t smraw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 127) & ~uintptr_t(127));
@@ -161,16 +168,16 @@ cudaError_t launch_gated_rmsnorm(const void *o, const void *z, const float *weig
     const bool bf = io_dtype == GDN_DT_BF16;
     const void *fn = bf ? reinterpret_cast<const void *>(k_gated_rmsnorm<__nv_bfloat16>)
                         : reinterpret_cast<const void *>(k_gated_rmsnorm<float>);
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+    const size_t smem = bf ? smem_bytes<__nv_bfloat16>() : smem_bytes<float>();
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
-    const long long rows_per_block = kBlockBytes / (kHeadDim * (bf ? 2 : 4));
-    const long long nblocks = (rows + rows_per_block - 1) / rows_per_block;
-    const unsigned grid = unsigned(nblocks < 2LL * sms ? nblocks : 2LL * sms);
+    const long long nblocks = (rows + kBlockRows - 1) / kBlockRows;
+    const unsigned grid = unsigned(nblocks < (long long)kCtasPerSm * sms ? nblocks : (long long)kCtasPerSm * sms);
     LaunchScope scope(GDN_K_GATED_RMSNORM, s);
     if (bf)
-        k_gated_rmsnorm<__nv_bfloat16><<<grid, kNThreads, kSmemBytes, s>>>(o, z, weight, eps, y, rows, status);
+        k_gated_rmsnorm<__nv_bfloat16><<<grid, kNThreads, smem, s>>>(o, z, weight, eps, y, rows, status);
     else
-        k_gated_rmsnorm<float><<<grid, kNThreads, kSmemBytes, s>>>(o, z, weight, eps, y, rows, status);
+        k_gated_rmsnorm<float><<<grid, kNThreads, smem, s>>>(o, z, weight, eps, y, rows, status);
     return cudaGetLastError();
 }
 
