@@ -39,6 +39,7 @@
 //   y = o / sqrt(mean(o^2) + eps) * weight * silu(z)
 // in f32 before the single rounding to the output dtype.
 #include "gdn_common.cuh"
+#include "tc_ptx.cuh"
 
 namespace gdn {
 namespace {
@@ -101,8 +102,17 @@ struct StateWords<__nv_bfloat16> {
     }
 };
 
+// bf16 state cache: the pair's 32 KiB state comes in by one bulk copy into
+// shared memory and is read from there where it is used, so that no
+// registers hold it in flight and four CTAs fit on an SM (128 KiB in flight
+// per SM). The f32 state keeps its words in registers (16 x 16 bytes per
+// thread, two CTAs per SM), which already streams at the copy rate.
+template <typename ST>
+constexpr bool kBulkState = sizeof(ST) == 2;
+constexpr uint32_t kBulkStateBytes = kHeadDim * kHeadDim * 2;
+
 template <typename T, typename ST, bool kFront, bool kGateOut>
-__global__ void __launch_bounds__(kRThreads, sizeof(ST) == 2 ? 3 : 2)
+__global__ void __launch_bounds__(kRThreads, kBulkState<ST> ? 4 : 2)
 k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const void *__restrict__ v,
                  const float *__restrict__ g, const float *__restrict__ beta, DecodeFront front, float scale,
                  void *__restrict__ state, const int32_t *__restrict__ idx, void *__restrict__ out,
@@ -111,6 +121,9 @@ k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const v
     __shared__ float4 red_p[kRThreads / 32][32], red_r[kRThreads / 32][32];
     __shared__ float qk_s, rk_s, rq_s, alpha_s, beta_s;
     __shared__ float4 gz_s[32];  // weight * silu(z), 4 channels per lane
+    __shared__ uint64_t st_bar;
+    extern __shared__ __align__(128) uint8_t st_sm[];  // bf16 cache: the pair's state [128][128]
+    constexpr bool kBulk = kBulkState<ST>;
     const int pair = blockIdx.x;
     const int n = pair / hv, h = pair % hv, hk = h / (hv / hq);
     const int tid = threadIdx.x, lane = tid & 31, wrow = tid >> 5;
@@ -121,6 +134,12 @@ k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const v
         return;
     }
     ST *S = static_cast<ST *>(state) + (size_t(slot) * hv + h) * kHeadDim * kHeadDim;
+    if (kBulk && tid == 0) {
+        tc::mbar_init(&st_bar, 1);
+        tc::fence_mbar_init();
+        tc::mbar_arrive_expect_tx(&st_bar, kBulkStateBytes);
+        tc::bulk_load(st_sm, S, kBulkStateBytes, &st_bar);
+    }
     // The small inputs are issued first, each by the warp that uses it, so that
     // they arrive while the 64 KiB state read is still in flight. Nothing but
     // the q/k staging stands before the first barrier: the front-end's scalar
@@ -151,10 +170,21 @@ k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const v
         kq_k = ldx<T>(k, qk_off);
         kq_q = ldx<T>(q, qk_off);
     }
-    // all state loads: 16 independent 128-bit loads per thread
-    typename StateWords<ST>::raw s[kRowsPerThread];
+    // f32 cache: all state loads, 16 independent 128-bit loads per thread
+    typename StateWords<ST>::raw s[kBulk ? 1 : kRowsPerThread];
+    if constexpr (!kBulk) {
 #pragma unroll
-    for (int i = 0; i < kRowsPerThread; ++i) s[i] = StateWords<ST>::load(S + size_t(wrow + 8 * i) * kHeadDim + 4 * lane);
+        for (int i = 0; i < kRowsPerThread; ++i)
+            s[i] = StateWords<ST>::load(S + size_t(wrow + 8 * i) * kHeadDim + 4 * lane);
+    }
+    // this thread's 4 columns of state row wrow + 8 i
+    auto state_row = [&](int i) -> float4 {
+        if constexpr (kBulk)
+            return StateWords<ST>::f(
+                StateWords<ST>::load(reinterpret_cast<const ST *>(st_sm) + size_t(wrow + 8 * i) * kHeadDim + 4 * lane));
+        else
+            return StateWords<ST>::f(s[i]);
+    };
     if (tid < kHeadDim) {
         ks[tid] = kq_k;
         qs[tid] = kq_q;
@@ -179,11 +209,18 @@ k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const v
     }
     if (gate_out && wrow == kZWarp)
         gz_s[lane] = make_float4(nw.x * silu_f(zz.x), nw.y * silu_f(zz.y), nw.z * silu_f(zz.z), nw.w * silu_f(zz.w));
+    if constexpr (kBulk) {  // the state copy has landed (a bounded wait; a timeout skips the pair)
+        const bool landed = tc::mbar_wait_spin(&st_bar, 0);
+        if (__syncthreads_or(!landed)) {
+            if (tid == 0) record_status(status, GDN_ETIMEOUT);
+            return;
+        }
+    }
     float4 p = make_float4(0.f, 0.f, 0.f, 0.f), r = p;
 #pragma unroll
     for (int i = 0; i < kRowsPerThread; ++i) {
         const float kd = ks[wrow + 8 * i], qd = qs[wrow + 8 * i];
-        const float4 si = StateWords<ST>::f(s[i]);
+        const float4 si = state_row(i);
         p.x = fmaf(kd, si.x, p.x); p.y = fmaf(kd, si.y, p.y);
         p.z = fmaf(kd, si.z, p.z); p.w = fmaf(kd, si.w, p.w);
         r.x = fmaf(qd, si.x, r.x); r.y = fmaf(qd, si.y, r.y);
@@ -243,7 +280,7 @@ k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const v
 #pragma unroll
     for (int i = 0; i < kRowsPerThread; ++i) {
         const float kd = ks[wrow + 8 * i];
-        const float4 si = StateWords<ST>::f(s[i]);
+        const float4 si = state_row(i);
         float4 t;
         t.x = fmaf(alpha, si.x, kd * d.x);
         t.y = fmaf(alpha, si.y, kd * d.y);
@@ -280,7 +317,8 @@ cudaError_t launch_recurrent_step(const gdn_problem &p, const void *q, const voi
         p.io_dtype == GDN_DT_BF16
             ? (st_bf ? pick_step<__nv_bfloat16, __nv_bfloat16>(front, gate) : pick_step<__nv_bfloat16, float>(front, gate))
             : (st_bf ? pick_step<float, __nv_bfloat16>(front, gate) : pick_step<float, float>(front, gate));
-    kern<<<pairs, kRThreads, 0, s>>>(q, k, v, g, beta, f, scale, state, state_indices, out, p.num_seqs, p.hq,
+    kern<<<pairs, kRThreads, st_bf ? kBulkStateBytes : 0, s>>>(q, k, v, g, beta, f, scale, state, state_indices, out,
+                                                              p.num_seqs, p.hq,
                                     p.hv, p.num_state_slots, (p.flags & GDN_FLAG_BETA_BF16) ? 1 : 0, status);
     return cudaGetLastError();
 }
