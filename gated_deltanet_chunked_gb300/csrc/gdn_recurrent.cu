@@ -104,7 +104,7 @@ struct StateWords<__nv_bfloat16> {
 
 // bf16 state cache: the pair's 32 KiB state comes in by one bulk copy into
 // shared memory and is read from there where it is used, so that no
-// registers hold it in flight and four CTAs fit on an SM (128 KiB in flight
+// registers hold it in flight and five CTAs fit on an SM (160 KiB in flight
 // per SM). The f32 state keeps its words in registers (16 x 16 bytes per
 // thread, two CTAs per SM), which already streams at the copy rate.
 template <typename ST>
@@ -112,7 +112,7 @@ constexpr bool kBulkState = sizeof(ST) == 2;
 constexpr uint32_t kBulkStateBytes = kHeadDim * kHeadDim * 2;
 
 template <typename T, typename ST, bool kFront, bool kGateOut>
-__global__ void __launch_bounds__(kRThreads, kBulkState<ST> ? 4 : 2)
+__global__ void __launch_bounds__(kRThreads, kBulkState<ST> ? 5 : 2)
 k_recurrent_step(const void *__restrict__ q, const void *__restrict__ k, const void *__restrict__ v,
                  const float *__restrict__ g, const float *__restrict__ beta, DecodeFront front, float scale,
                  void *__restrict__ state, const int32_t *__restrict__ idx, void *__restrict__ out,
