@@ -544,12 +544,13 @@ __device__ __forceinline__ void prep_unit(const PrefillArgs &a, const TcWs &w, c
     }
     ld_phase ^= 1;
     // publish the unit: the plain stores of every engine thread are ordered
-    // before the flag by the barrier, the bulk copies completed above
+    // before the flag by the barrier and the release store's gpu-scope fence
+    // (a sequentially consistent fence on top cost ~2 us here); the bulk
+    // copies completed above, the proxy fence orders them before the flag
     tc_fence_before();
     ebar();
     if (tid == 0 && !s.abort) {
         fence_proxy_async_global();
-        __threadfence();
         st_release_gpu(w.ready + unit, 1);
     }
 }
@@ -1000,12 +1001,11 @@ k_chunk_fused_tc(FusedArgs fa, const __grid_constant__ CUtensorMap tm_q, const _
         const int nprep = int(gridDim.x) - fa.n_state;
         // engine e of prepare CTA i takes units k * 3 * nprep + e * nprep + i:
         // the first chunks go to engine 0 of every CTA, which starts at once;
-        // engines 1 and 2 start 3 and 6 us later, so that the engines sharing
+        // engines 1 and 2 start 1.5 and 3 us later, so that the engines sharing
         // an SM stay out of step and their load waits overlap the others' work
-        if (e > 0) {
+        if (e > 0) {  // asleep, so as not to take issue slots from engine 0's first units
             const uint64_t t0 = globaltimer_ns();
-            while (globaltimer_ns() - t0 < uint64_t(e) * 3000ull) {
-            }
+            while (globaltimer_ns() - t0 < uint64_t(e) * 1500ull) __nanosleep(500);
         }
         for (int u = e * nprep + (int(blockIdx.x) - fa.n_state); u < units && !s.abort; u += kEngines * nprep)
             prep_unit(a, w, &tm_q, &tm_k, &tm_v, s, tmem + 128 * e, 1 + e, ld_phase, mma_phase, u / a.hv, u % a.hv);
@@ -1025,8 +1025,10 @@ size_t prefill_tc_workspace(int max_chunks, int hv) {
 int *prefill_tc_ready_flags(void *ws_data, int max_chunks, int hv) { return tc_carve(ws_data, max_chunks, hv).ready; }
 
 // CTAs that walk: the split that minimises the larger of the two estimated
-// times (a walk step ~1.7 us, an engine unit ~17 us, measured at T=4096),
-// with the chunks of a sequence estimated from the mean length.
+// times, with the chunks of a sequence estimated from the mean length.
+// Measured at T=4096: a walk step ~1.4 us, ~5 us per walk beyond its steps,
+// ~14 us until the first chunks are prepared, an engine unit ~17 us with
+// three engines busy on an SM.
 static int state_ctas(const PrefillArgs &a, int ctas) {
     const int walks = a.num_seqs * a.hv;
     const double steps = double(a.total_tokens) / (double(kChunk) * (a.num_seqs > 0 ? a.num_seqs : 1)) + 2.0;
@@ -1034,7 +1036,7 @@ static int state_ctas(const PrefillArgs &a, int ctas) {
     int best = 1;
     double best_t = 1e300;
     for (int n = 1; n < ctas && n <= walks; ++n) {
-        const double t_walk = double((walks + n - 1) / n) * steps * 1.7;
+        const double t_walk = 14.0 + double((walks + n - 1) / n) * (steps * 1.4 + 5.0);
         const double t_prep = std::ceil(units / (double(ctas - n) * kEngines)) * 17.0;
         const double t = t_walk > t_prep ? t_walk : t_prep;
         if (t < best_t) {
