@@ -191,3 +191,44 @@ def test_conv_step_out_of_range_slot(cuda):
                                     state_indices=torch.tensor([1, 5], dtype=torch.int32, device=cuda))
     assert gdn.gdn_read_device_status(clear=True) == gdn.GDN_EDEVICE_INPUT
     assert torch.equal(st[0], st0[0].to(cuda))  # slot 0 is nobody's
+
+
+@pytest.mark.parametrize("state_bf16", [False, True], ids=["f32state", "bf16state"])
+def test_decode_layer_core_from_projections(cuda, state_bf16):
+    """Eight decode steps of the layer core from raw projections, as the
+    SGLang decode path runs it: conv step (no norm) -> gated recurrent step
+    (q/k norm, gates, output gate in one kernel), against the oracle's
+    convolution, gated step and gated RMSNorm; optionally with the bf16 state
+    cache and bf16 beta."""
+    hq, hv, N = 2, 4, 5
+    dtype = torch.bfloat16
+    _, w, b, cst0 = W.make_conv_inputs(80, 1, hq, hv, dtype, slots=N)
+    wl = W.Workload("dec_layer", 81, "decode", dtype, hq=hq, hv=hv, num_seqs=N, s0_sigma=0.05)
+    A_log, dt_bias = W.make_decode_gate_params(wl)
+    S0 = W.make_decode_state(wl)
+    if state_bf16:
+        S0 = S0.to(torch.bfloat16)
+    idx = torch.tensor([3, 0, 4, 1, 2], dtype=torch.int32)
+    cst, S = cst0.to(cuda), S0.to(cuda)
+    cst_ref, S_ref = cst0.double().numpy(), S0.double().numpy()
+    cu = np.arange(N + 1)
+    rng = np.random.default_rng(82)
+    for step in range(8):
+        x, _, _, _ = W.make_conv_inputs(900 + step, N, hq, hv, dtype)
+        a = torch.from_numpy(rng.standard_normal((N, hv)).astype(np.float32))
+        bb = torch.from_numpy(rng.standard_normal((N, hv)).astype(np.float32))
+        z, nw = W.make_output_gate(900 + step, N, hv, dtype)
+        q, k, v = gdn.gdn_causal_conv1d_silu_step(x.to(cuda), w.to(cuda), hq, hv, bias=b.to(cuda), conv_state=cst,
+                                                  state_indices=idx.to(cuda))
+        y = gdn.gdn_recurrent_step_gated(q, k, v, a.to(cuda), bb.to(cuda), A_log.to(cuda), dt_bias.to(cuda),
+                                         128 ** -0.5, S, state_indices=idx.to(cuda), z=z.to(cuda),
+                                         norm_weight=nw.to(cuda), norm_eps=1e-6, beta_bf16=state_bf16)
+        torch.cuda.synchronize()
+        y_c, cst_ref = oracle.causal_conv1d_silu(x, w, b, cst_ref, cu, idx.numpy())
+        q_r, k_r, v_r = split_ref(y_c, hq, hv)
+        o_r, S_ref = oracle.recurrent_step_gated(q_r, k_r, v_r, a, bb, A_log, dt_bias, 128 ** -0.5, S_ref, idx.numpy(),
+                                                 beta_bf16=state_bf16, state_bf16=state_bf16)
+        check(y, oracle.gated_rmsnorm(o_r, z, nw, 1e-6), dtype, f"y step {step}")
+    assert gdn.gdn_read_device_status() == gdn.GDN_OK
+    check(S, S_ref, dtype, "recurrent state after 8 steps")
+    check(cst, cst_ref, dtype, "conv state after 8 steps")
