@@ -16,8 +16,8 @@
 //
 // k_conv1d_silu: a thread owns 4 consecutive channels (one 8- or 16-byte
 // access per token), so a warp covers exactly one 128-channel head and the
-// q/k norm is one warp reduction. A CTA (grid x: token tiles, y: channel
-// blocks) takes 1024 channels over a tile of tokens of the packed token axis
+// q/k norm is one warp reduction. A CTA (linear grid, the channel block
+// varying fastest) takes 1024 channels over a tile of tokens of the packed token axis
 // and slides the window down it in registers. The tile's rows of x (2 KiB per
 // token for bf16) come into shared memory by bulk copies issued at once by one
 // thread, so that a whole tile is in flight per CTA without holding
@@ -72,7 +72,7 @@ struct ConvArgs {
     const int32_t *idx;       // [N] or null
     const int32_t *cu;        // [N+1] or null (one sequence)
     void *oq, *ok, *ov;       // [T, hq, 128], [T, hq, 128], [T, hv, 128]
-    int T, C, N, slots, hq, hv, tile, norm_qk;
+    int T, C, N, slots, hq, hv, tile, norm_qk, cblocks;
     int *status;
 };
 
@@ -105,7 +105,9 @@ __global__ void __launch_bounds__(kCThreads) k_conv1d_silu(ConvArgs a) {
     __shared__ uint64_t bar;
     __shared__ int abort_flag;
     const int lane = threadIdx.x & 31;
-    const int c0 = blockIdx.y * kCPerBlock + threadIdx.x * kCPerThread;
+    // channel block fastest: CTAs that run together cover whole token rows
+    const int cblock = int(blockIdx.x % a.cblocks), ctile = int(blockIdx.x / a.cblocks);
+    const int c0 = cblock * kCPerBlock + threadIdx.x * kCPerThread;
     const int32_t one_seq[2] = {0, a.T};
     const int32_t *cu = a.cu ? a.cu : one_seq;
     const int N = a.cu ? a.N : 1;
@@ -118,13 +120,13 @@ __global__ void __launch_bounds__(kCThreads) k_conv1d_silu(ConvArgs a) {
             return;
         }
     }
-    const int t_nominal = int(blockIdx.x) * a.tile;
+    const int t_nominal = ctile * a.tile;
     const int t_begin = tile_start(cu, N, a.T, t_nominal);
     const int t_end = tile_start(cu, N, a.T, min(t_nominal + a.tile, a.T));
     if (t_begin >= t_end) return;  // uniform over the CTA
     const T *X = static_cast<const T *>(a.x);
     // the tile's rows of x for these 1024 channels, by bulk copies (one per token)
-    const int cb0 = blockIdx.y * kCPerBlock;
+    const int cb0 = cblock * kCPerBlock;
     const uint32_t row_bytes = uint32_t(min(kCPerBlock, a.C - cb0)) * sizeof(T);
     if (threadIdx.x == 0) {
         mbar_init(&bar, 1);
@@ -214,6 +216,36 @@ __global__ void __launch_bounds__(kCThreads) k_conv1d_silu(ConvArgs a) {
         st4v<T>(dst + size_t(t) * drow + dcol, y);
         h0 = h1, h1 = h2, h2 = xv;
     };
+    // four tokens at once: their windows [h0 h1 h2 x0], [h1 h2 x0 x1],
+    // [h2 x0 x1 x2], [x0 x1 x2 x3] and four independent norm reductions
+    auto conv1 = [&](const float4 &a0, const float4 &a1, const float4 &a2, const float4 &a3) {
+        float4 y;
+        y.x = silu_f(fmaf(w[3].x, a3.x, fmaf(w[2].x, a2.x, fmaf(w[1].x, a1.x, fmaf(w[0].x, a0.x, bias.x)))));
+        y.y = silu_f(fmaf(w[3].y, a3.y, fmaf(w[2].y, a2.y, fmaf(w[1].y, a1.y, fmaf(w[0].y, a0.y, bias.y)))));
+        y.z = silu_f(fmaf(w[3].z, a3.z, fmaf(w[2].z, a2.z, fmaf(w[1].z, a1.z, fmaf(w[0].z, a0.z, bias.z)))));
+        y.w = silu_f(fmaf(w[3].w, a3.w, fmaf(w[2].w, a2.w, fmaf(w[1].w, a1.w, fmaf(w[0].w, a0.w, bias.w)))));
+        return y;
+    };
+    auto emit4 = [&](int t, const float4 &x0, const float4 &x1, const float4 &x2, const float4 &x3) {
+        float4 y[4] = {conv1(h0, h1, h2, x0), conv1(h1, h2, x0, x1), conv1(h2, x0, x1, x2), conv1(x0, x1, x2, x3)};
+        if (norm) {
+            float ss[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) ss[j] = y[j].x * y[j].x + y[j].y * y[j].y + y[j].z * y[j].z + y[j].w * y[j].w;
+#pragma unroll
+            for (int m = 16; m; m >>= 1)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) ss[j] += __shfl_xor_sync(0xffffffffu, ss[j], m);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float inv = rsqrtf(ss[j] + 1e-6f);
+                y[j].x *= inv; y[j].y *= inv; y[j].z *= inv; y[j].w *= inv;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) st4v<T>(dst + size_t(t + j) * drow + dcol, y[j]);
+        h0 = x1, h1 = x2, h2 = x3;
+    };
     load_history(t_begin);
     const bool landed = mbar_wait(&bar, 0);
     if (!__all_sync(0xffffffffu, landed)) {
@@ -228,6 +260,10 @@ __global__ void __launch_bounds__(kCThreads) k_conv1d_silu(ConvArgs a) {
             load_history(t);
         }
         const int run_end = min(t_end, s_end);  // tokens of sequence s in this tile
+        for (; t + 4 <= run_end; t += 4) {
+            const T *xr = XS + size_t(t - t_begin) * kCPerBlock;
+            emit4(t, ld4v<T>(xr), ld4v<T>(xr + kCPerBlock), ld4v<T>(xr + 2 * kCPerBlock), ld4v<T>(xr + 3 * kCPerBlock));
+        }
         for (; t < run_end; ++t) emit(t, ld4v<T>(XS + size_t(t - t_begin) * kCPerBlock));
     }
 }
@@ -313,8 +349,10 @@ cudaError_t launch_conv1d_silu(const gdn_problem &p, const void *x, const float 
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     ConvArgs a{x, weight, bias, conv_state, state_indices, cu_seqlens, out_q, out_k, out_v,
-               p.total_tokens, C, p.num_seqs, p.num_state_slots, p.hq, p.hv, tile, norm_qk, status};
-    const dim3 grid((p.total_tokens + tile - 1) / tile, cblocks);
+               p.total_tokens, C, p.num_seqs, p.num_state_slots, p.hq, p.hv, tile, norm_qk, cblocks, status};
+    const long long nblk = (long long)((p.total_tokens + tile - 1) / tile) * cblocks;
+    if (nblk >= (1ll << 31)) return cudaErrorInvalidConfiguration;
+    const unsigned grid = unsigned(nblk);
     LaunchScope scope(GDN_K_CONV1D_SILU, s);
     if (p.io_dtype == GDN_DT_BF16) k_conv1d_silu<__nv_bfloat16><<<grid, kCThreads, smem, s>>>(a);
     else k_conv1d_silu<float><<<grid, kCThreads, smem, s>>>(a);
@@ -327,7 +365,7 @@ cudaError_t launch_conv1d_step(const gdn_problem &p, const void *x, const float 
     const int C = (2 * p.hq + p.hv) * kHeadDim;
     if (p.num_seqs == 0) return cudaSuccess;
     ConvArgs a{x, weight, bias, conv_state, state_indices, nullptr, out_q, out_k, out_v,
-               p.num_seqs, C, p.num_seqs, p.num_state_slots, p.hq, p.hv, 1, norm_qk, status};
+               p.num_seqs, C, p.num_seqs, p.num_state_slots, p.hq, p.hv, 1, norm_qk, 1, status};
     const dim3 grid(p.num_seqs, (C + kCPerBlock - 1) / kCPerBlock);
     LaunchScope scope(GDN_K_CONV1D_STEP, s);
     if (p.io_dtype == GDN_DT_BF16) k_conv1d_step<__nv_bfloat16><<<grid, kCThreads, 0, s>>>(a);
