@@ -99,7 +99,8 @@ const char *gdn_status_string(int status) {
         case GDN_ECUDA: return "GDN_ECUDA: a CUDA runtime call or kernel launch failed";
         case GDN_ETIMEOUT: return "GDN_ETIMEOUT: a bounded device-side wait gave up";
         case GDN_EDEVICE_INPUT: return "GDN_EDEVICE_INPUT: device-side input check failed (cu_seqlens or slot index)";
-        case GDN_ETOOBIG: return "GDN_ETOOBIG: workspace need exceeds the fixed no-alloc scratch (GDN_NOALLOC_SCRATCH_BYTES)";
+        case GDN_ETOOBIG:
+            return "GDN_ETOOBIG: workspace need exceeds the fixed no-alloc scratch (GDN_NOALLOC_SCRATCH_BYTES)";
         default: return "unknown gdn_status";
     }
 }

@@ -315,7 +315,8 @@ cudaError_t launch_recurrent_step(const gdn_problem &p, const void *q, const voi
     const bool st_bf = (p.flags & GDN_FLAG_STATE_BF16) != 0;
     const StepKernel kern =
         p.io_dtype == GDN_DT_BF16
-            ? (st_bf ? pick_step<__nv_bfloat16, __nv_bfloat16>(front, gate) : pick_step<__nv_bfloat16, float>(front, gate))
+            ? (st_bf ? pick_step<__nv_bfloat16, __nv_bfloat16>(front, gate)
+                     : pick_step<__nv_bfloat16, float>(front, gate))
             : (st_bf ? pick_step<float, __nv_bfloat16>(front, gate) : pick_step<float, float>(front, gate));
     kern<<<pairs, kRThreads, st_bf ? kBulkStateBytes : 0, s>>>(q, k, v, g, beta, f, scale, state, state_indices, out,
                                                               p.num_seqs, p.hq,
