@@ -922,7 +922,9 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
             }
             warp_arrive(&s.emptyM[b]);
         }
-        if (lane == 0) bulk_wait_group_all();  // output stores complete before the CTA exits
+        // the output stores have read their staging buffers (the next walk
+        // reuses them, and the CTA may exit); their writes complete with the grid
+        if (lane == 0) bulk_wait_group_read<0>();
     }
     tc_fence_before();
     __syncthreads();
