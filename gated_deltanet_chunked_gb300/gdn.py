@@ -123,6 +123,13 @@ def _io_dtype(t: torch.Tensor) -> int:
     raise ValueError(f"unsupported io dtype {t.dtype}")
 
 
+def _want(dtype, **tensors):
+    """Raises ValueError unless every given (non-None) tensor has ``dtype``."""
+    for name, t in tensors.items():
+        if t is not None and t.dtype != dtype:
+            raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
 def _stream(stream) -> ctypes.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -154,6 +161,9 @@ def gdn_chunk_fwd(q, k, v, g, beta, scale, initial_state=None, cu_seqlens=None, 
     """
     packed = cu_seqlens is not None
     num_seqs = cu_seqlens.numel() - 1 if packed else q.shape[0]
+    _want(q.dtype, k=k, v=v, out=out)
+    _want(torch.float32, g=g, beta=beta, initial_state=initial_state, final_state=final_state)
+    _want(torch.int32, cu_seqlens=cu_seqlens)
     prob = prefill_problem(q, v, num_seqs, packed)
     if out is None:
         out = torch.empty(v.shape, dtype=v.dtype, device=v.device)
@@ -179,6 +189,9 @@ def gdn_chunk_fwd_noalloc(q, k, v, g, beta, scale, out, final_state=None, initia
     supplied. Raises GdnError(GDN_ETOOBIG) for problems above that size."""
     packed = cu_seqlens is not None
     num_seqs = cu_seqlens.numel() - 1 if packed else q.shape[0]
+    _want(q.dtype, k=k, v=v, out=out)
+    _want(torch.float32, g=g, beta=beta, initial_state=initial_state, final_state=final_state)
+    _want(torch.int32, cu_seqlens=cu_seqlens)
     prob = prefill_problem(q, v, num_seqs, packed)
     st = load().gdn_chunk_fwd_noalloc(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                                       ctypes.c_float(scale), _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
@@ -197,6 +210,11 @@ def gdn_recurrent_step(q, k, v, g, beta, scale, state, state_indices=None, out=N
     """One decode step; ``state`` [slots, Hv, 128, 128] (f32, or bf16 for a
     bf16 state cache) is updated in place. ``beta_bf16`` rounds beta to bf16."""
     N, hq, dk = q.shape
+    _want(q.dtype, k=k, v=v, out=out)
+    _want(torch.float32, g=g, beta=beta)
+    _want(torch.int32, state_indices=state_indices)
+    if state.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError(f"state must be float32 or bfloat16, got {state.dtype}")
     prob = GdnProblem(N, 1, N, N, hq, v.shape[1], dk, v.shape[2], _io_dtype(q), _decode_flags(state, beta_bf16),
                       state.shape[0])
     if out is None:
@@ -217,6 +235,11 @@ def gdn_recurrent_step_gated(q, k, v, a, b, A_log, dt_bias, scale, state, state_
     (head-wise RMSNorm, then silu(z)) is applied before the store. A bf16
     ``state`` is a bf16 state cache; ``beta_bf16`` rounds beta to bf16."""
     N, hq, dk = q.shape
+    _want(q.dtype, k=k, v=v, out=out, z=z)
+    _want(torch.float32, a=a, b=b, A_log=A_log, dt_bias=dt_bias, norm_weight=norm_weight)
+    _want(torch.int32, state_indices=state_indices)
+    if state.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError(f"state must be float32 or bfloat16, got {state.dtype}")
     prob = GdnProblem(N, 1, N, N, hq, v.shape[1], dk, v.shape[2], _io_dtype(q), _decode_flags(state, beta_bf16),
                       state.shape[0])
     if out is None:
@@ -234,6 +257,8 @@ def gdn_gated_rmsnorm(o, z, weight, eps, out=None, stream=None):
     """y = o / sqrt(mean(o^2) + eps) * weight * silu(z) per (token, head) row
     of o, z [T, Hv, 128] (io dtype) with weight [128] f32. ``out`` may be o."""
     T, hv, dv = o.shape
+    _want(o.dtype, z=z, out=out)
+    _want(torch.float32, weight=weight)
     prob = GdnProblem(1, 0, 1, T, 1, hv, dv, dv, _io_dtype(o), 0, 0)
     if out is None:
         out = torch.empty_like(o)
@@ -254,6 +279,9 @@ def gdn_causal_conv1d_silu(x, weight, hq, hv, bias=None, conv_state=None, state_
     if C != (2 * hq + hv) * 128:
         raise ValueError("x must have (2 hq + hv) * 128 channels")
     N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    _want(x.dtype, conv_state=conv_state, q=q, k=k, v=v)
+    _want(torch.float32, weight=weight, bias=bias)
+    _want(torch.int32, state_indices=state_indices, cu_seqlens=cu_seqlens)
     slots = 0 if conv_state is None else conv_state.shape[0]
     prob = GdnProblem(1, 0, N, T, hq, hv, 128, 128, _io_dtype(x), 0, slots)
     q = torch.empty((T, hq, 128), dtype=x.dtype, device=x.device) if q is None else q
@@ -273,6 +301,9 @@ def gdn_causal_conv1d_silu_step(x, weight, hq, hv, bias=None, conv_state=None, s
     N, C = x.shape
     if C != (2 * hq + hv) * 128:
         raise ValueError("x must have (2 hq + hv) * 128 channels")
+    _want(x.dtype, conv_state=conv_state, q=q, k=k, v=v)
+    _want(torch.float32, weight=weight, bias=bias)
+    _want(torch.int32, state_indices=state_indices)
     slots = 0 if conv_state is None else conv_state.shape[0]
     prob = GdnProblem(N, 1, N, N, hq, hv, 128, 128, _io_dtype(x), 0, slots)
     q = torch.empty((N, hq, 128), dtype=x.dtype, device=x.device) if q is None else q
@@ -289,6 +320,7 @@ def gdn_causal_conv1d_silu_step(x, weight, hq, hv, bias=None, conv_state=None, s
 def gdn_gating(a, b, A_log, dt_bias, g=None, beta=None, stream=None):
     """g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b), a, b [T, Hv] f32."""
     T, hv = a.shape
+    _want(torch.float32, a=a, b=b, A_log=A_log, dt_bias=dt_bias, g=g, beta=beta)
     prob = GdnProblem(1, 0, 1, T, 1, hv, 128, 128, GDN_DT_F32, 0, 0)
     g = torch.empty_like(a) if g is None else g
     beta = torch.empty_like(a) if beta is None else beta

@@ -182,3 +182,25 @@ def test_conv_and_gating_reject_bad_arguments():
     assert gating(problem(hv=0)) == gdn.GDN_EINVAL
     assert gating(problem(), a=0) == gdn.GDN_EINVAL
     assert gating(problem(), g=FAKE + 2) == gdn.GDN_EINVAL
+
+
+def test_binding_rejects_wrong_dtypes():
+    """The binding checks dtypes before any call (no GPU needed)."""
+    import torch
+
+    bf = torch.bfloat16
+    q = torch.zeros((2, 1, 128), dtype=bf)
+    v = torch.zeros((2, 2, 128), dtype=bf)
+    g = torch.zeros((2, 2))
+    with pytest.raises(ValueError):
+        gdn.gdn_recurrent_step(q, q, v, g, g.double(), 0.1, torch.zeros((2, 2, 128, 128)))
+    with pytest.raises(ValueError):
+        gdn.gdn_recurrent_step(q, q, v, g, g, 0.1, torch.zeros((2, 2, 128, 128), dtype=torch.float16))
+    with pytest.raises(ValueError):
+        gdn.gdn_chunk_fwd(q, q, v.float(), g, g, 0.1)
+    with pytest.raises(ValueError):
+        gdn.gdn_gated_rmsnorm(v, v.float(), torch.ones(128), 1e-6)
+    with pytest.raises(ValueError):
+        gdn.gdn_causal_conv1d_silu(torch.zeros((2, 512), dtype=bf), torch.zeros((512, 4), dtype=bf), 1, 2)
+    with pytest.raises(ValueError):
+        gdn.gdn_gating(g, g, torch.zeros(2, dtype=torch.float64), torch.zeros(2))
