@@ -14,7 +14,8 @@ front-end and the output gate computed in the kernel) under "decode_gated",
 and that with a bf16 state cache and bf16 beta under "decode_sglang";
 the stand-alone output gate (gdn_gated_rmsnorm) over the prefill's
 [4096, 32, 128] read-out under "output_gate"; the short convolution (prefill
-projections and one decode step) and the gating under "front_end".
+projections and one decode step) and the gating under "front_end"; the prefill
+step with the output gate fused in (gdn_chunk_fwd_gated) under "prefill_gated".
 
 Multi-GPU (torchrun, one rank per GPU): every rank runs its own replica of the
 workload (weak scaling: the GDN core shards over sequences and heads with no
@@ -388,6 +389,7 @@ def run_ours(args, world, rank, local):
     decode_sglang = None if args.no_decode else run_decode(args, dev, world, peaks, peak_src, gated=True,
                                                            sglang=True)
     output_gate = None if args.no_decode else run_gate_norm(args, dev, world, peaks, peak_src)
+    prefill_gated = None if args.no_decode else run_prefill_gated(args, dev, world)
     front_end = None if args.no_decode else run_front_end(args, dev, world, peaks, peak_src)
     clocks.stop()
     clk = clocks.summary(t_start, t_end)
@@ -406,7 +408,7 @@ def run_ours(args, world, rank, local):
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": gpu_launches,
         "kernels": kernels, "decode": decode, "decode_gated": decode_gated, "decode_sglang": decode_sglang,
         "output_gate": output_gate,
-        "front_end": front_end,
+        "front_end": front_end, "prefill_gated": prefill_gated,
         "step_ms": {"median": statistics.median(step_ms), "p10": sorted(step_ms)[len(step_ms) // 10],
                     "p90": sorted(step_ms)[(9 * len(step_ms)) // 10]},
     }
@@ -483,6 +485,46 @@ def run_decode(args, dev, world, peaks, peak_src, gated=False, sglang=False):
                      "peak_source": f"{peak_src} (hbm_gbs, burst copy)"},
         "l2": f"state ({state.numel() * state.element_size() / 1e6:.0f} MB) larger than L2; no flush",
     }
+
+
+def run_prefill_gated(args, dev, world):
+    """Times the T=4096 prefill step with the output gate fused in
+    (gdn_chunk_fwd_gated) the way the main line times the plain step."""
+    from gated_deltanet_chunked_gb300 import gdn
+
+    w = PREFILL
+    host = W.make_prefill(w)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+    z, weight = (t.to(dev) for t in W.make_output_gate(w.seed, w.seqlen, w.hv, w.io_dtype))
+    T = host["total_tokens"]
+    out = torch.empty_like(d["v"])
+    fin = torch.empty((1, w.hv, 128, 128), dtype=torch.float32, device=dev)
+    prob = gdn.prefill_problem(d["q"], d["v"], 1, packed=True)
+    ws = torch.empty(gdn.gdn_chunk_fwd_workspace_size(prob), dtype=torch.uint8, device=dev)
+    cu = torch.tensor([0, T], dtype=torch.int32, device=dev)
+    flush = L2Flush(dev)
+
+    def step():
+        gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], cu_seqlens=cu, out=out,
+                          final_state=fin, workspace=ws, z=z, norm_weight=weight, norm_eps=1e-6)
+
+    for _ in range(max(3, args.warmup)):
+        flush()
+        step()
+    steps = max(10, min(args.steps, 100))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for a, b in ev:
+        flush()
+        a.record()
+        step()
+        b.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev) / steps, world, dev)
+    return {"workload": f"{w.name} + output gate", "ms_per_step": ms, "value": world * T / (ms * 1e-3),
+            "unit": "tokens/s", "l2": L2_NOTE,
+            "what": "prefill with RMSNorm(o) * weight * silu(z) applied in the fused kernel (gdn_chunk_fwd_gated)"}
 
 
 def run_gate_norm(args, dev, world, peaks, peak_src):

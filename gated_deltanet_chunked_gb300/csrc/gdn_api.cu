@@ -59,6 +59,8 @@ int check_prefill_shape(const gdn_problem *p, bool packed) {
     // token-row products must stay addressable with 64-bit offsets and the
     // chunk count must fit the int32 chunk table
     if (int64_t(p->total_tokens) / kChunk + p->num_seqs > (int64_t(1) << 30)) return GDN_EINVAL;
+    // the per-(chunk, head) flags and counters are indexed with int
+    if ((int64_t(p->total_tokens) / kChunk + p->num_seqs) * p->hv * 2 >= (int64_t(1) << 31)) return GDN_EINVAL;
     return GDN_OK;
 }
 
@@ -112,9 +114,21 @@ size_t gdn_chunk_fwd_workspace_size(const gdn_problem *p) {
     return ws_layout(p).total;
 }
 
-int gdn_chunk_fwd(const gdn_problem *p, const void *q, const void *k, const void *v, const float *g,
-                  const float *beta, float scale, const float *initial_state, const int32_t *cu_seqlens,
-                  void *out, float *final_state, void *workspace, size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace gdn {
+namespace {
+
+// The output gate of gdn_chunk_fwd_gated (null z: none).
+struct OutGate {
+    const void *z;
+    const float *weight;
+    float eps;
+};
+
+int chunk_fwd(const gdn_problem *p, const void *q, const void *k, const void *v, const float *g, const float *beta,
+              float scale, const float *initial_state, const int32_t *cu_seqlens, const OutGate &gate, void *out,
+              float *final_state, void *workspace, size_t workspace_bytes, void *stream) {
     const bool packed = cu_seqlens != nullptr;
     int st = check_prefill_shape(p, packed);
     if (st) return st;
@@ -148,12 +162,45 @@ int gdn_chunk_fwd(const gdn_problem *p, const void *q, const void *k, const void
     a.status = status;
     if (p->io_dtype == GDN_DT_BF16) {
         a.ready = prefill_tc_ready_flags(ws + L.data_off, a.max_chunks, a.hv);
-        a.ready_count = a.max_chunks * a.hv;
+        a.done = a.ready + size_t(a.max_chunks) * a.hv;  // output counters follow the ready flags
+        a.ready_count = 2 * a.max_chunks * a.hv;
+    }
+    if (gate.z) {
+        if (p->total_tokens > 0 && (!aligned16(gate.z) || !gate.weight || !aligned16(gate.weight))) return GDN_EINVAL;
+        if (!(gate.eps >= 0.f)) return GDN_EINVAL;
+        a.z = gate.z;
+        a.norm_weight = gate.weight;
+        a.norm_eps = gate.eps;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if ((st = cuda_status(launch_chunk_table(a, s)))) return st;
     if (p->io_dtype == GDN_DT_BF16) return cuda_status(launch_prefill_tc(a, ws + L.data_off, s));
-    return cuda_status(launch_prefill_simt(a, ws + L.data_off, s));
+    if ((st = cuda_status(launch_prefill_simt(a, ws + L.data_off, s)))) return st;
+    if (!gate.z) return GDN_OK;
+    return cuda_status(launch_gated_rmsnorm(out, gate.z, gate.weight, gate.eps, out,
+                                            (long long)p->total_tokens * p->hv, p->io_dtype, status, s));
+}
+
+}  // namespace
+}  // namespace gdn
+
+extern "C" {
+
+int gdn_chunk_fwd(const gdn_problem *p, const void *q, const void *k, const void *v, const float *g,
+                  const float *beta, float scale, const float *initial_state, const int32_t *cu_seqlens,
+                  void *out, float *final_state, void *workspace, size_t workspace_bytes, void *stream) {
+    return gdn::chunk_fwd(p, q, k, v, g, beta, scale, initial_state, cu_seqlens, gdn::OutGate{nullptr, nullptr, 0.f},
+                          out, final_state, workspace, workspace_bytes, stream);
+}
+
+int gdn_chunk_fwd_gated(const gdn_problem *p, const void *q, const void *k, const void *v, const float *g,
+                        const float *beta, float scale, const float *initial_state, const int32_t *cu_seqlens,
+                        const void *z, const float *norm_weight, float norm_eps, void *out, float *final_state,
+                        void *workspace, size_t workspace_bytes, void *stream) {
+    if (!z) return GDN_EINVAL;
+    return gdn::chunk_fwd(p, q, k, v, g, beta, scale, initial_state, cu_seqlens,
+                          gdn::OutGate{z, norm_weight, norm_eps}, out, final_state, workspace, workspace_bytes,
+                          stream);
 }
 
 constexpr uint32_t kDecodeFlags = GDN_FLAG_BETA_BF16 | GDN_FLAG_STATE_BF16;

@@ -571,7 +571,7 @@ __device__ __forceinline__ void prep_unit(const PrefillArgs &a, const TcWs &w, c
 // into the prepared Q and P tiles).
 constexpr int kMathThreads = 256;   // 8 warps: lane quarter (warp % 4) x column half (warp / 4),
                                     // then a copy warp (one polling thread) and an MMA warp
-constexpr int kCopyWarpB = 8, kMmaWarp = 9, kCopyWarpM = 10;
+constexpr int kCopyWarpB = 8, kMmaWarp = 9, kCopyWarpM = 10, kPublishWarp = 11;
 
 // tensor-memory columns (512 allocated)
 constexpr uint32_t kTmSig = 0;    // Sigma accumulator f32 [e][k], 128 columns
@@ -600,6 +600,7 @@ struct StateSmem {
     uint64_t fullB[2], emptyB[2], fullM[2], emptyM[2], ready_s, ready_x, mma, mma_o;
     uint32_t tmem;
     int abort;
+    int outc[8];  // output gate on: chunks of this walk whose block of math warp w is in memory
 };
 
 static_assert(sizeof(BStage) % 1024 == 0 && sizeof(MStage) % 1024 == 0, "stages keep the swizzle alignment");
@@ -634,6 +635,7 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
         mbar_init(&s.ready_x, kMathThreads / 32);
         mbar_init(&s.mma, 1);
         mbar_init(&s.mma_o, 1);
+        for (int i = 0; i < kMathThreads / 32; ++i) s.outc[i] = 0;
         fence_mbar_init();
     }
     tc_fence_before();
@@ -760,6 +762,31 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
                 if (uses > 0) mbar_wait(&s.emptyB[b], (uses - 1) & 1, 100000000ull);
             }
         }
+    } else if (warp == kPublishWarp) {
+        // ----------------------- output publication -------------------------
+        // output gate on: chunks whose 8 blocks are all in memory are counted
+        // in the workspace for the gate engines, with one gpu-scope release
+        if (a.z && lane == 0 && nc > 0) {
+            int published = 0;
+            const uint64_t t0 = globaltimer_ns();
+            while (published < nc && !*reinterpret_cast<volatile int *>(&s.abort)) {
+                int m = nc;
+                for (int i = 0; i < kMathThreads / 32; ++i)
+                    m = min(m, *reinterpret_cast<volatile int *>(&s.outc[i]));
+                if (m > published) {
+                    __threadfence_block();
+                    fence_proxy_async_global();
+                    for (int cc = published; cc < m; ++cc)
+                        red_release_add_gpu(a.done + size_t(si.first_chunk + cc) * a.hv + h, kMathThreads / 32);
+                    published = m;
+                } else if (globaltimer_ns() - t0 > 2000000000ull) {
+                    s.abort = 1;
+                    break;
+                } else {
+                    __nanosleep(200);
+                }
+            }
+        }
     } else if (warp < kMathThreads / 32) {
         // --------------------------- math warps ----------------------------
         const int lq = warp & 3, ch = warp >> 2;  // TMEM lane quarter, column half
@@ -767,6 +794,25 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
         const uint32_t lrow = uint32_t(32 * lq) << 16;
         const int last_len = si.len - kChunk * (nc - 1);  // valid length of the last chunk
         const size_t orow = size_t(a.hv) * kHeadDim;      // output row stride (elements)
+        // one of the 8 math warps' blocks of chunk cc is in memory: every
+        // lane's plain stores (warp barrier) and the completed store groups
+        // (all but the newest when this step issued one) are ordered before
+        // the release increment the output-gate engines acquire
+        // `newer`: store groups committed after chunk cc's (they may stay
+        // pending). Only a CTA-scope counter here: the gpu-scope release (a
+        // fence of ~1 us) is the publishing warp's, off the step's chain.
+        auto publish_out = [&](int cc, int newer) {
+            __syncwarp();
+            if (lane == 0) {
+                if (newer >= 2) bulk_wait_group<2>();
+                else if (newer == 1) bulk_wait_group<1>();
+                else bulk_wait_group<0>();
+                __threadfence_block();
+                *reinterpret_cast<volatile int *>(&s.outc[warp]) = cc + 1;
+            }
+            __syncwarp();
+        };
+        bool tma_prev = false;  // the previous step committed a store group
         // state columns k = 64 ch .. 64 ch + 63 of row e: Sigma_-1 = S0^T
         {
             float v[64];
@@ -879,6 +925,7 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
                 s.abort = 1;
                 break;
             }
+            bool stored_tma = false;  // this step committed a store group
             if (c >= 0) {
                 // O_c rows r = 32 ch + j, column e
                 // a 2x2 transpose between lanes e and e^1 on packed pairs: each lane
@@ -911,6 +958,7 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
                         tma_store_3d(tm_o, 32 * lq, h, row0, blk);
                         bulk_commit_group();
                     }
+                    stored_tma = true;
                 } else {
                     __nv_bfloat16 *obase =
                         static_cast<__nv_bfloat16 *>(a.out) + (size_t(row0 + odd) * a.hv + h) * kHeadDim + (e & ~1);
@@ -920,7 +968,16 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
                             *reinterpret_cast<uint32_t *>(obase + size_t(2 * m) * orow) = pr[m];
                 }
             }
+            // output gate on: this warp's block of chunk c-2 has landed (its store
+            // group, issued two steps ago, completed; waiting on the previous
+            // step's group instead held every step up): count it
+            if (a.z && c >= 2) publish_out(c - 2, int(stored_tma) + int(tma_prev));
+            tma_prev = stored_tma;
             warp_arrive(&s.emptyM[b]);
+        }
+        if (a.z && !__any_sync(0xffffffffu, s.abort)) {
+            if (nc >= 2) publish_out(nc - 2, 0);
+            if (nc >= 1) publish_out(nc - 1, 0);
         }
         // the output stores have read their staging buffers (the next walk
         // reuses them, and the CTA may exit); their writes complete with the grid
@@ -930,6 +987,79 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
     __syncthreads();
     tc_fence_after();
     if (s.abort && tid == 0) record_status(a.status, GDN_ETIMEOUT);
+}
+
+// ===========================================================================
+// gate_unit: the output gate of one (chunk, v-head) tile, in place
+// ===========================================================================
+// y = o / sqrt(mean(o^2) + eps) * weight * silu(z) over each token's 128
+// channels (the sgl-qwen3-5-moe page's output_rmsnorm_silu_gate), run by a
+// prepare engine after its last unit, once the walk's 8 math warps have each
+// counted their block of the chunk as written. Each warp of the engine waits
+// for the count itself (bounded), acquires it, and takes rows w, w+4, ...,
+// 4 channels per lane.
+__device__ __forceinline__ bool gate_unit(const PrefillArgs &a, int c, int h, int etid) {
+    const int lane = etid & 31, ew = etid >> 5;
+    const int *cnt = a.done + size_t(c) * a.hv + h;
+    bool ok = true;
+    if (lane == 0) {
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_gpu(cnt) < kMathThreads / 32) {
+            if (globaltimer_ns() - t0 > 2000000000ull) {
+                ok = false;
+                break;
+            }
+            __nanosleep(500);
+        }
+    }
+    if (!__shfl_sync(0xffffffffu, ok, 0)) return false;
+    (void)ld_acquire_gpu(cnt);  // every lane acquires what the walk released
+    const ChunkInfo ci = a.chunk_info[c];
+    const float4 wt = reinterpret_cast<const float4 *>(a.norm_weight)[lane];
+    uint2 *O = static_cast<uint2 *>(a.out);
+    const uint2 *Z = static_cast<const uint2 *>(a.z);
+    const size_t rstride = size_t(a.hv) * (kHeadDim / 4);  // uint2 (4 bf16) per row of the tensor
+    const size_t col = size_t(h) * (kHeadDim / 4) + lane;
+    // warp ew takes rows ew, ew + 4, ... (16 of the chunk's 64): all 32 loads
+    // are issued before any arithmetic, so a tile costs about one round trip
+    constexpr int kRows = kChunk / (kPrepThreads / 32);
+    uint2 ov[kRows], zv[kRows];
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) {
+        const int r = min(ew + 4 * j, ci.len - 1);  // rows past the chunk: recomputed, not stored
+        const size_t off = size_t(ci.start + r) * rstride + col;
+        ov[j] = O[off];
+        zv[j] = Z[off];
+    }
+#pragma unroll
+    for (int j4 = 0; j4 < kRows; j4 += 4) {
+        float4 x[4], gz[4];
+        float ss[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 o0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ov[j4 + j].x));
+            const float2 o1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ov[j4 + j].y));
+            const float2 z0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&zv[j4 + j].x));
+            const float2 z1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&zv[j4 + j].y));
+            x[j] = make_float4(o0.x, o0.y, o1.x, o1.y);
+            gz[j] = make_float4(wt.x * silu_f(z0.x), wt.y * silu_f(z0.y), wt.z * silu_f(z1.x), wt.w * silu_f(z1.y));
+            ss[j] = x[j].x * x[j].x + x[j].y * x[j].y + x[j].z * x[j].z + x[j].w * x[j].w;
+        }
+#pragma unroll
+        for (int m = 16; m; m >>= 1)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) ss[j] += __shfl_xor_sync(0xffffffffu, ss[j], m);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int r = ew + 4 * (j4 + j);
+            if (r >= ci.len) continue;
+            const float inv = rsqrtf(ss[j] * (1.f / kHeadDim) + a.norm_eps);
+            O[size_t(ci.start + r) * rstride + col] =
+                make_uint2(pack_bf16x2(x[j].x * inv * gz[j].x, x[j].y * inv * gz[j].y),
+                           pack_bf16x2(x[j].z * inv * gz[j].z, x[j].w * inv * gz[j].w));
+        }
+    }
+    return true;
 }
 
 // ===========================================================================
@@ -1011,6 +1141,17 @@ k_chunk_fused_tc(FusedArgs fa, const __grid_constant__ CUtensorMap tm_q, const _
         }
         for (int u = e * nprep + (int(blockIdx.x) - fa.n_state); u < units && !s.abort; u += kEngines * nprep)
             prep_unit(a, w, &tm_q, &tm_k, &tm_v, s, tmem + 128 * e, 1 + e, ld_phase, mma_phase, u / a.hv, u % a.hv);
+        // then the output gate of the same units, in chunk order, as the walks
+        // finish them (the walks never wait for this)
+        if (a.z && !s.abort) {
+            const int etid = tid & (kPrepThreads - 1);
+            for (int u = e * nprep + (int(blockIdx.x) - fa.n_state); u < units; u += kEngines * nprep) {
+                if (!gate_unit(a, u / a.hv, u % a.hv, etid)) {
+                    if ((etid & 31) == 0) record_status(a.status, GDN_ETIMEOUT);
+                    break;
+                }
+            }
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -1021,7 +1162,7 @@ k_chunk_fused_tc(FusedArgs fa, const __grid_constant__ CUtensorMap tm_q, const _
 
 size_t prefill_tc_workspace(int max_chunks, int hv) {
     const size_t units = size_t(max_chunks) * hv;
-    return al256(units * kUnitBytes) + al256(units * 128 * sizeof(float)) + al256(units * sizeof(int));
+    return al256(units * kUnitBytes) + al256(units * 128 * sizeof(float)) + al256(2 * units * sizeof(int));
 }
 
 int *prefill_tc_ready_flags(void *ws_data, int max_chunks, int hv) { return tc_carve(ws_data, max_chunks, hv).ready; }

@@ -47,7 +47,12 @@ struct PrefillArgs {
     ChunkInfo *chunk_info;  // [max_chunks]
     int *status;  // device status word
     int *ready;       // per-unit ready flags of the tensor-core path (zeroed by the chunk table), or null
-    int ready_count;
+    int ready_count;  // flags the chunk table zeroes (ready flags, then the output counters)
+    // optional output gate (z null: none): out = RMSNorm(o) * weight * silu(z)
+    const void *z;
+    const float *norm_weight;
+    float norm_eps;
+    int *done;        // per-unit count of math warps whose output block has landed (tensor-core path)
 };
 
 __device__ __forceinline__ void record_status(int *status, int code) {

@@ -28,7 +28,7 @@ GDN_FLAG_BETA_BF16, GDN_FLAG_STATE_BF16 = 1 << 1, 1 << 2
 SYMBOLS = ("gdn_chunk_fwd", "gdn_chunk_fwd_workspace_size", "gdn_recurrent_step", "gdn_read_device_status",
            "gdn_status_string", "gdn_version", "gdn_profile_enable", "gdn_profile_collect", "gdn_kernel_name",
            "gdn_chunk_fwd_noalloc", "gdn_recurrent_step_gated", "gdn_gated_rmsnorm", "gdn_causal_conv1d_silu",
-           "gdn_gating", "gdn_causal_conv1d_silu_step")
+           "gdn_gating", "gdn_causal_conv1d_silu_step", "gdn_chunk_fwd_gated")
 GDN_K_COUNT = 11
 
 
@@ -60,6 +60,9 @@ def load(path: Optional[str] = None):
             lib.gdn_chunk_fwd.argtypes = [P, _vp, _vp, _vp, _fp, _fp, ctypes.c_float, _fp, _ip, _vp, _fp, _vp,
                                           ctypes.c_size_t, _vp]
             lib.gdn_chunk_fwd.restype = ctypes.c_int
+            lib.gdn_chunk_fwd_gated.argtypes = [P, _vp, _vp, _vp, _fp, _fp, ctypes.c_float, _fp, _ip, _vp, _fp,
+                                                ctypes.c_float, _vp, _fp, _vp, ctypes.c_size_t, _vp]
+            lib.gdn_chunk_fwd_gated.restype = ctypes.c_int
             lib.gdn_chunk_fwd_workspace_size.argtypes = [P]
             lib.gdn_chunk_fwd_workspace_size.restype = ctypes.c_size_t
             lib.gdn_recurrent_step.argtypes = [P, _vp, _vp, _vp, _fp, _fp, ctypes.c_float, _fp, _ip, _vp, _vp]
@@ -153,16 +156,20 @@ def gdn_chunk_fwd_workspace_size(problem: GdnProblem) -> int:
 
 
 def gdn_chunk_fwd(q, k, v, g, beta, scale, initial_state=None, cu_seqlens=None, out=None,
-                  final_state=None, output_final_state=True, workspace=None, stream=None):
+                  final_state=None, output_final_state=True, workspace=None, stream=None,
+                  z=None, norm_weight=None, norm_eps=1e-6):
     """Chunked prefill. Packed when ``cu_seqlens`` (int32 device [N+1]) is given.
 
     Returns (out, final_state). ``workspace`` (uint8 device tensor) is
-    allocated with PyTorch when not supplied.
+    allocated with PyTorch when not supplied. With ``z`` (like v) and
+    ``norm_weight`` [128] f32, out holds the output gate applied to the
+    read-out (gdn_chunk_fwd_gated).
     """
     packed = cu_seqlens is not None
     num_seqs = cu_seqlens.numel() - 1 if packed else q.shape[0]
-    _want(q.dtype, k=k, v=v, out=out)
-    _want(torch.float32, g=g, beta=beta, initial_state=initial_state, final_state=final_state)
+    _want(q.dtype, k=k, v=v, out=out, z=z)
+    _want(torch.float32, g=g, beta=beta, initial_state=initial_state, final_state=final_state,
+          norm_weight=norm_weight)
     _want(torch.int32, cu_seqlens=cu_seqlens)
     prob = prefill_problem(q, v, num_seqs, packed)
     if out is None:
@@ -172,12 +179,20 @@ def gdn_chunk_fwd(q, k, v, g, beta, scale, initial_state=None, cu_seqlens=None, 
     need = gdn_chunk_fwd_workspace_size(prob)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=v.device)
-    st = load().gdn_chunk_fwd(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
-                              ctypes.c_float(scale), _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
-                              _ptr(final_state), _ptr(workspace), ctypes.c_size_t(workspace.numel()),
-                              _stream(stream))
+    if z is None:
+        st = load().gdn_chunk_fwd(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                  ctypes.c_float(scale), _ptr(initial_state), _ptr(cu_seqlens), _ptr(out),
+                                  _ptr(final_state), _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                                  _stream(stream))
+        where = "gdn_chunk_fwd"
+    else:
+        st = load().gdn_chunk_fwd_gated(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                        ctypes.c_float(scale), _ptr(initial_state), _ptr(cu_seqlens), _ptr(z),
+                                        _ptr(norm_weight), ctypes.c_float(norm_eps), _ptr(out), _ptr(final_state),
+                                        _ptr(workspace), ctypes.c_size_t(workspace.numel()), _stream(stream))
+        where = "gdn_chunk_fwd_gated"
     if st != GDN_OK:
-        raise GdnError(st, "gdn_chunk_fwd")
+        raise GdnError(st, where)
     return out, final_state
 
 

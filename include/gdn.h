@@ -132,6 +132,25 @@ int gdn_chunk_fwd(const gdn_problem *p, const void *q, const void *k, const void
                   void *out, float *final_state,
                   void *workspace, size_t workspace_bytes, void *stream);
 
+/* gdn_chunk_fwd followed by the layer's output gate ([SGL] node
+ * output_rmsnorm_silu_gate; the gated-RMSNorm row of [Kestrel]): out receives,
+ * for every token t and v-head h,
+ *   y[t,h] = o[t,h] / sqrt(mean_j o[t,h,j]^2 + norm_eps) * norm_weight * silu(z[t,h])
+ * where o is what gdn_chunk_fwd would have written (rounded to the io dtype
+ * first, as [SGL]'s node reads it). The other arguments and results are
+ * gdn_chunk_fwd's (same workspace size).
+ *   z           [total_tokens, hv, 128] io dtype, 16-byte aligned (not NULL)
+ *   norm_weight [128] f32, 16-byte aligned; norm_eps >= 0
+ * The bf16 path applies the gate inside its fused kernel, on the prepare
+ * CTAs once their units are done, tile by tile as the walks finish them; the
+ * f32 path runs the gdn_gated_rmsnorm pass after its output kernel. */
+int gdn_chunk_fwd_gated(const gdn_problem *p, const void *q, const void *k, const void *v,
+                        const float *g, const float *beta, float scale,
+                        const float *initial_state, const int32_t *cu_seqlens,
+                        const void *z, const float *norm_weight, float norm_eps,
+                        void *out, float *final_state,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
 /* Bytes of the static device scratch array behind gdn_chunk_fwd_noalloc. */
 #define GDN_NOALLOC_SCRATCH_BYTES (32u << 20)
 
