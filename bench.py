@@ -15,7 +15,9 @@ and that with a bf16 state cache and bf16 beta under "decode_sglang";
 the stand-alone output gate (gdn_gated_rmsnorm) over the prefill's
 [4096, 32, 128] read-out under "output_gate"; the short convolution (prefill
 projections and one decode step) and the gating under "front_end"; the prefill
-step with the output gate fused in (gdn_chunk_fwd_gated) under "prefill_gated".
+step with the output gate fused in (gdn_chunk_fwd_gated) under "prefill_gated";
+the plain prefill on 8 packed sequences of U[100, 8000] tokens with initial
+states and on one T=65536 sequence under "prefill_configs".
 
 Multi-GPU (torchrun, one rank per GPU): every rank runs its own replica of the
 workload (weak scaling: the GDN core shards over sequences and heads with no
@@ -390,6 +392,8 @@ def run_ours(args, world, rank, local):
                                                            sglang=True)
     output_gate = None if args.no_decode else run_gate_norm(args, dev, world, peaks, peak_src)
     prefill_gated = None if args.no_decode else run_prefill_gated(args, dev, world)
+    prefill_configs = None if (args.no_decode or args.no_configs) else run_prefill_configs(args, dev, world, peaks,
+                                                                                           peak_src)
     front_end = None if args.no_decode else run_front_end(args, dev, world, peaks, peak_src)
     clocks.stop()
     clk = clocks.summary(t_start, t_end)
@@ -408,7 +412,7 @@ def run_ours(args, world, rank, local):
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": gpu_launches,
         "kernels": kernels, "decode": decode, "decode_gated": decode_gated, "decode_sglang": decode_sglang,
         "output_gate": output_gate,
-        "front_end": front_end, "prefill_gated": prefill_gated,
+        "front_end": front_end, "prefill_gated": prefill_gated, "prefill_configs": prefill_configs,
         "step_ms": {"median": statistics.median(step_ms), "p10": sorted(step_ms)[len(step_ms) // 10],
                     "p90": sorted(step_ms)[(9 * len(step_ms)) // 10]},
     }
@@ -487,6 +491,62 @@ def run_decode(args, dev, world, peaks, peak_src, gated=False, sglang=False):
     }
 
 
+def run_prefill_configs(args, dev, world, peaks, peak_src):
+    """Times the plain prefill on the two other prefill workloads: 8 packed
+    sequences of U[100, 8000] tokens with initial states, and one T=65536
+    sequence. Each reports its step time, tokens/s and the fraction of the
+    path's roofline max(bytes / HBM peak, FLOPs / bf16 peak), as the main
+    line does for T=4096."""
+    from gated_deltanet_chunked_gb300 import gdn
+
+    res = {}
+    flush = L2Flush(dev)
+    for name in ("varlen_8seq_hq16_hv32", "long_T65536_hq16_hv32"):
+        w = W.WORKLOADS[name]
+        host = W.make_prefill(w)
+        T, N = host["total_tokens"], host["num_seqs"]
+        d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in host.items()}
+        cu = d["cu_seqlens"] if d.get("cu_seqlens") is not None else torch.tensor([0, T], dtype=torch.int32,
+                                                                                   device=dev)
+        lens = (cu[1:] - cu[:-1]).tolist()
+        s0 = d.get("initial_state")
+        out = torch.empty_like(d["v"])
+        fin = torch.empty((N, w.hv, 128, 128), dtype=torch.float32, device=dev)
+        prob = gdn.prefill_problem(d["q"], d["v"], N, packed=True)
+        ws = torch.empty(gdn.gdn_chunk_fwd_workspace_size(prob), dtype=torch.uint8, device=dev)
+
+        def step():
+            gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], initial_state=s0,
+                              cu_seqlens=cu, out=out, final_state=fin, workspace=ws)
+
+        for _ in range(max(3, args.warmup)):
+            flush()
+            step()
+        torch.cuda.synchronize()
+        assert gdn.gdn_read_device_status() == gdn.GDN_OK
+        steps = max(5, min(args.steps, 30))
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        barrier(world)
+        torch.cuda.synchronize()
+        for a, b in ev:
+            flush()
+            a.record()
+            step()
+            b.record()
+        torch.cuda.synchronize()
+        ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev) / steps, world, dev)
+        nbytes = prefill_bytes(T, N, w.hq, w.hv, s0=s0 is not None)
+        flops = prefill_flops(sum(math.ceil(n / 64) for n in lens) * w.hv, w.hv, w.hq)
+        t_roof = max(nbytes / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
+        res[name] = {"ms_per_step": ms, "value": world * T / (ms * 1e-3), "unit": "tokens/s", "tokens": T,
+                     "sequences": N, "longest": max(lens), "initial_state": s0 is not None,
+                     "path_bytes": nbytes, "path_flops": flops, "roofline_us": t_roof * 1e6,
+                     "frac_of_roofline": t_roof / (ms * 1e-3), "peak_source": peak_src, "l2": L2_NOTE}
+        del d, out, fin, ws, host
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_prefill_gated(args, dev, world):
     """Times the T=4096 prefill step with the output gate fused in
     (gdn_chunk_fwd_gated) the way the main line times the plain step."""
@@ -523,7 +583,7 @@ def run_prefill_gated(args, dev, world):
     torch.cuda.synchronize()
     ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev) / steps, world, dev)
     return {"workload": f"{w.name} + output gate", "ms_per_step": ms, "value": world * T / (ms * 1e-3),
-            "unit": "tokens/s", "l2": L2_NOTE,
+            "unit": "tokens/s", "l2": L2_NOTE, "traffic": ncu_traffic("chunk_fused_tc_gated"),
             "what": "prefill with RMSNorm(o) * weight * silu(z) applied in the fused kernel (gdn_chunk_fwd_gated)"}
 
 
@@ -712,6 +772,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the varlen and T=65536 prefill legs")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -246,11 +246,6 @@ __device__ __forceinline__ void prep_unit(const PrefillArgs &a, const TcWs &w, c
     if (!ok_kq) s.abort = 1;
     mma_phase ^= 1;
     tc_fence_after();
-    // the Q slots are free: V_c goes there for U^T (needed only after the solve)
-    if (tid == 0 && !s.abort) {
-        mbar_arrive_expect_tx(&s.bar_v, 2 * kTile);
-        for (int hf = 0; hf < 2; ++hf) tma_load_3d(s.KQ + hf * 2 * kTile + kTile, tm_v, 64 * hf, h, ci.start, &s.bar_v);
-    }
     // ---- M (rows 0-63: K K^T) and P (rows 64-127: Q K^T), one row per thread ----
     if (ok_kq) {
         float v[64];
@@ -295,6 +290,14 @@ __device__ __forceinline__ void prep_unit(const PrefillArgs &a, const TcWs &w, c
     }
     tc_fence_before();
     ebar();
+    // the Q slots are free now that every warp has copied its share of the
+    // scaled Q tile (the barrier above): V_c goes there for U^T, needed only
+    // after the solve. Issued before that barrier, the load could overwrite
+    // rows a slower warp had still to copy.
+    if (tid == 0 && !s.abort) {
+        mbar_arrive_expect_tx(&s.bar_v, 2 * kTile);
+        for (int hf = 0; hf < 2; ++hf) tma_load_3d(s.KQ + hf * 2 * kTile + kTile, tm_v, 64 * hf, h, ci.start, &s.bar_v);
+    }
     if (tid < 64) s.gc[tid] = exp_decay(s.gc[tid]);  // gc -> gamma (read only by the A diag(beta gamma) step)
     // ---- A = (I + M)^-1, 16x16 blocks ----
 
