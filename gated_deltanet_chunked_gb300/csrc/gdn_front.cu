@@ -155,6 +155,11 @@ __global__ void __launch_bounds__(kCThreads) k_conv1d_silu(ConvArgs a) {
         w[3] = make_float4(r[0].w, r[1].w, r[2].w, r[3].w);
     }
     const float4 bias = a.bias ? *reinterpret_cast<const float4 *>(a.bias + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
+    // taps and bias as channel pairs (0, 1) and (2, 3) for the packed f32x2 arithmetic
+    float2 wl[kConvK], wh[kConvK];
+#pragma unroll
+    for (int j = 0; j < kConvK; ++j) wl[j] = make_float2(w[j].x, w[j].y), wh[j] = make_float2(w[j].z, w[j].w);
+    const float2 bl = make_float2(bias.x, bias.y), bh = make_float2(bias.z, bias.w);
     // output tensor and column of these channels
     const int qk_c = a.hq * kHeadDim;
     T *dst;
@@ -201,12 +206,24 @@ __global__ void __launch_bounds__(kCThreads) k_conv1d_silu(ConvArgs a) {
             }
         }
     };
+    // one token's 4 channels: taps oldest first, bias innermost, then SiLU,
+    // two channels per packed f32x2 operation (the same result per channel;
+    // measured 41.8 -> 40.4 us on the T=4096 projections)
+    auto conv1 = [&](const float4 &a0, const float4 &a1, const float4 &a2, const float4 &a3) {
+        float2 lo = __ffma2_rn(wl[3], make_float2(a3.x, a3.y),
+                               __ffma2_rn(wl[2], make_float2(a2.x, a2.y),
+                                          __ffma2_rn(wl[1], make_float2(a1.x, a1.y),
+                                                     __ffma2_rn(wl[0], make_float2(a0.x, a0.y), bl))));
+        float2 hi = __ffma2_rn(wh[3], make_float2(a3.z, a3.w),
+                               __ffma2_rn(wh[2], make_float2(a2.z, a2.w),
+                                          __ffma2_rn(wh[1], make_float2(a1.z, a1.w),
+                                                     __ffma2_rn(wh[0], make_float2(a0.z, a0.w), bh))));
+        lo = silu2_f(lo);
+        hi = silu2_f(hi);
+        return make_float4(lo.x, lo.y, hi.x, hi.y);
+    };
     auto emit = [&](int t, const float4 &xv) {
-        float4 y;
-        y.x = silu_f(fmaf(w[3].x, xv.x, fmaf(w[2].x, h2.x, fmaf(w[1].x, h1.x, fmaf(w[0].x, h0.x, bias.x)))));
-        y.y = silu_f(fmaf(w[3].y, xv.y, fmaf(w[2].y, h2.y, fmaf(w[1].y, h1.y, fmaf(w[0].y, h0.y, bias.y)))));
-        y.z = silu_f(fmaf(w[3].z, xv.z, fmaf(w[2].z, h2.z, fmaf(w[1].z, h1.z, fmaf(w[0].z, h0.z, bias.z)))));
-        y.w = silu_f(fmaf(w[3].w, xv.w, fmaf(w[2].w, h2.w, fmaf(w[1].w, h1.w, fmaf(w[0].w, h0.w, bias.w)))));
+        float4 y = conv1(h0, h1, h2, xv);
         if (norm) {
             float ss = y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
             for (int m = 16; m; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
@@ -218,14 +235,6 @@ __global__ void __launch_bounds__(kCThreads) k_conv1d_silu(ConvArgs a) {
     };
     // four tokens at once: their windows [h0 h1 h2 x0], [h1 h2 x0 x1],
     // [h2 x0 x1 x2], [x0 x1 x2 x3] and four independent norm reductions
-    auto conv1 = [&](const float4 &a0, const float4 &a1, const float4 &a2, const float4 &a3) {
-        float4 y;
-        y.x = silu_f(fmaf(w[3].x, a3.x, fmaf(w[2].x, a2.x, fmaf(w[1].x, a1.x, fmaf(w[0].x, a0.x, bias.x)))));
-        y.y = silu_f(fmaf(w[3].y, a3.y, fmaf(w[2].y, a2.y, fmaf(w[1].y, a1.y, fmaf(w[0].y, a0.y, bias.y)))));
-        y.z = silu_f(fmaf(w[3].z, a3.z, fmaf(w[2].z, a2.z, fmaf(w[1].z, a1.z, fmaf(w[0].z, a0.z, bias.z)))));
-        y.w = silu_f(fmaf(w[3].w, a3.w, fmaf(w[2].w, a2.w, fmaf(w[1].w, a1.w, fmaf(w[0].w, a0.w, bias.w)))));
-        return y;
-    };
     auto emit4 = [&](int t, const float4 &x0, const float4 &x1, const float4 &x2, const float4 &x3) {
         float4 y[4] = {conv1(h0, h1, h2, x0), conv1(h1, h2, x0, x1), conv1(h2, x0, x1, x2), conv1(x0, x1, x2, x3)};
         if (norm) {
