@@ -24,9 +24,9 @@ workload (weak scaling: the GDN core shards over sequences and heads with no
 exchange); a barrier brackets the timed region and the slowest rank's time is
 taken.
 
---impl reference times the CPU oracle (plain C, float64, OpenMP) on the same
-workload: each step runs a bounded sample (a quarter of the q/k head groups)
-and the rate is scaled to the whole workload.
+--impl reference times the CPU oracle (plain C, float64, OpenMP on every host
+core) on the same workload: each step is one chunk-form pass over all tokens
+and all heads, and the line reports the median step.
 """
 from __future__ import annotations
 
@@ -297,7 +297,7 @@ def run_ours(args, world, rank, local):
     gdn.gdn_profile_enable(False)
     prof = gdn.gdn_profile_collect(reset=True)
     step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
-    ms_local = sum(step_ms) / len(step_ms)
+    ms_local = statistics.median(step_ms)
     ms = max_over_ranks(ms_local, world, dev)
     value = world * T / (ms * 1e-3)
 
@@ -400,8 +400,13 @@ def run_ours(args, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(host, w, fraction=0.5)
+        cpu = cpu_baseline(host, w)
 
+    # One JSON line. The headline keys come first and the decode figures
+    # (half of the metric) last, with the f32-state decode as the final key,
+    # so that a reader keeping only the line's tail still sees them; the
+    # per-kernel tables and secondary legs are compact unless --detail.
+    r3 = lambda x: None if x is None else round(x, 4)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -409,13 +414,36 @@ def run_ours(args, world, rank, local):
         "config": {"workload": w.name, "B": 1, "T": T, "hq": w.hq, "hv": w.hv, "dk": 128, "dv": 128,
                    "chunk": 64, "initial_state": "zero", "final_state": "f32",
                    "l2": L2_NOTE, "parallelism": f"replicas x{world}"},
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": gpu_launches,
-        "kernels": kernels, "decode": decode, "decode_gated": decode_gated, "decode_sglang": decode_sglang,
-        "output_gate": output_gate,
-        "front_end": front_end, "prefill_gated": prefill_gated, "prefill_configs": prefill_configs,
-        "step_ms": {"median": statistics.median(step_ms), "p10": sorted(step_ms)[len(step_ms) // 10],
-                    "p90": sorted(step_ms)[(9 * len(step_ms)) // 10]},
+        "step_ms": {"median": statistics.median(step_ms), "mean": statistics.mean(step_ms),
+                    "p10": sorted(step_ms)[len(step_ms) // 10], "p90": sorted(step_ms)[(9 * len(step_ms)) // 10]},
+        "roofline": roofline, "e2e": e2e, "clocks": clk, "gpu_launches": gpu_launches,
+        "kernels_ms": {k: r3(v["ms_per_launch"]) for k, v in kernels.items()},
+        "cpu_baseline": cpu,
     }
+    if args.detail:
+        line.update({"kernels": kernels, "front_end": front_end, "output_gate": output_gate})
+    else:
+        line["front_end_frac"] = None if front_end is None else {
+            k: r3(v["roofline"]["frac"]) for k, v in front_end.items() if isinstance(v, dict) and "roofline" in v}
+        line["output_gate_frac"] = None if output_gate is None else r3(output_gate["roofline"]["frac"])
+    line["prefill_gated"] = None if prefill_gated is None else (
+        prefill_gated if args.detail else {"ms_per_step": prefill_gated["ms_per_step"], "value": prefill_gated["value"]})
+    line["prefill_configs"] = None if prefill_configs is None else (
+        prefill_configs if args.detail else {
+            k: {"ms_per_step": v["ms_per_step"], "value": v["value"], "roofline_us": r3(v["roofline_us"]),
+                "frac_of_roofline": r3(v["frac_of_roofline"])} for k, v in prefill_configs.items()})
+
+    def compact_decode(x):
+        if x is None or args.detail:
+            return x
+        rf = x["roofline"]
+        return {"ms_per_step": x["ms_per_step"], "value": x["value"], "unit": x["unit"],
+                "roofline": {"kernel": rf["kernel"], "achieved": rf["achieved"], "peak": rf["peak"],
+                             "frac": rf["frac"], "traffic": rf["traffic"]}}
+
+    line["decode_sglang"] = compact_decode(decode_sglang)
+    line["decode_gated"] = compact_decode(decode_gated)
+    line["decode"] = compact_decode(decode)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -702,33 +730,79 @@ def run_front_end(args, dev, world, peaks, peak_src):
     return res
 
 
-def cpu_baseline(host, w, fraction, min_seconds=10.0, max_passes=50):
-    """Times the CPU oracle (chunk form) on a bounded sample of the workload:
-    the first `fraction` of the q/k head groups, all tokens, repeated pass
-    after pass until at least `min_seconds` of CPU work have been timed."""
+def cpu_model():
+    """The host CPU's model name (from /proc/cpuinfo; Arm hosts may list only
+    implementer/part numbers) and the processor count."""
+    name = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        for key in ("model name", "Model name", "Hardware", "CPU part"):
+            for line in info.splitlines():
+                if line.split(":")[0].strip() == key:
+                    name = line.split(":", 1)[1].strip()
+                    break
+            if name:
+                break
+    except OSError:
+        pass
+    return {"model": name or "unknown", "nproc": os.cpu_count()}
+
+
+def _oracle_rate(fn, host, nk, G, min_seconds, max_passes=50):
+    """Tokens/s of one oracle routine over all tokens of the first nk q/k head
+    groups (nk * G v-heads), scaled to the whole workload by the head
+    fraction, with whole passes repeated until `min_seconds` have passed."""
+    T = host["total_tokens"]
+    q, k = host["q"][:, :nk], host["k"][:, :nk]
+    v, g, beta = host["v"][:, :nk * G], host["g"][:, :nk * G], host["beta"][:, :nk * G]
+    passes, t0 = 0, time.perf_counter()
+    while passes < max_passes and (passes == 0 or time.perf_counter() - t0 < min_seconds):
+        fn(q, k, v, g, beta, host["scale"], None, [0, T])
+        passes += 1
+    dt = time.perf_counter() - t0
+    hq = host["q"].shape[1]
+    return {"tokens_per_s": passes * T * (nk / hq) / dt, "passes": passes, "seconds": dt,
+            "v_heads": nk * G}
+
+
+def cpu_baseline(host, w, min_seconds=2.5):
+    """The CPU oracle as it stands on this host's cores: the token-by-token
+    recurrence (R) and the chunk form (Ch), each on one thread and on every
+    core. One thread runs a sample of one q/k head group (2 of 32 v-heads,
+    all tokens); all cores run every head. Rates are whole-workload tokens/s
+    (the one-thread sample scaled by its head fraction). `value` is Ch on all
+    cores, the routine and setting the reference arm times."""
     import oracle
 
     G = w.hv // w.hq
-    nk = max(1, int(w.hq * fraction))
-    q, k = host["q"][:, :nk], host["k"][:, :nk]
-    v, g, beta = host["v"][:, :nk * G], host["g"][:, :nk * G], host["beta"][:, :nk * G]
-    T = host["total_tokens"]
     oracle.build()
-    passes, t0 = 0, time.perf_counter()
-    while passes < max_passes and (passes == 0 or time.perf_counter() - t0 < min_seconds):
-        oracle.chunked(q, k, v, g, beta, host["scale"], None, [0, T])
-        passes += 1
-    dt = time.perf_counter() - t0
-    frac = nk / w.hq
-    return {"value": passes * T * frac / dt, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"chunk-form oracle (f64) over all {T} tokens of {nk}/{w.hq} q/k head groups "
-                      f"({nk * G}/{w.hv} v-heads), {passes} passes in {dt:.1f} s; rate scaled by the head fraction"}
+    procs = oracle.num_procs()
+    legs = {}
+    for threads, nk in ((1, 1), (procs, w.hq)):
+        oracle.set_threads(threads)
+        for name, fn in (("R", oracle.recurrent), ("Ch", oracle.chunked)):
+            legs[f"{name}_{'1thread' if threads == 1 else 'all_cores'}"] = {
+                **_oracle_rate(fn, host, nk, G, min_seconds), "threads": threads}
+    oracle.set_threads(procs)
+    best = legs["Ch_all_cores"]
+    T = host["total_tokens"]
+    return {"value": best["tokens_per_s"], "unit": "tokens/s", "cores": procs, "kind": "oracle",
+            "cpu": cpu_model(),
+            "sample": (f"f64 oracle on this host: R and Ch over all {T} tokens; one thread on 1 of {w.hq} q/k head "
+                       f"groups ({G} v-heads, rate scaled by the head fraction), all {procs} cores on all "
+                       f"{w.hv} v-heads; passes repeated for >= {min_seconds} s each; value = Ch on all cores"),
+            "legs": {k: {"tokens_per_s": v["tokens_per_s"], "threads": v["threads"], "v_heads": v["v_heads"],
+                         "passes": v["passes"], "seconds": round(v["seconds"], 2)} for k, v in legs.items()}}
 
 
 # --------------------------------------------------------------------------
 # reference arm: the CPU oracle as it stands
 # --------------------------------------------------------------------------
 def run_reference(args, world, rank):
+    """Times the chunk-form oracle (f64, OpenMP on every host core) on the
+    whole T=4096 workload, every head, once per step: ms_per_step is the
+    measured time of what ran, value the median step's tokens/s."""
     if rank != 0:
         return
     import oracle
@@ -736,29 +810,31 @@ def run_reference(args, world, rank):
     w = PREFILL
     host = W.make_prefill(w)
     T = host["total_tokens"]
-    G = w.hv // w.hq
-    nk = max(1, w.hq // 2)
-    q, k = host["q"][:, :nk], host["k"][:, :nk]
-    v, g, beta = host["v"][:, :nk * G], host["g"][:, :nk * G], host["beta"][:, :nk * G]
     oracle.build()
+    procs = oracle.num_procs()
+    oracle.set_threads(procs)
+    run = lambda: oracle.chunked(host["q"], host["k"], host["v"], host["g"], host["beta"], host["scale"], None,
+                                 [0, T])
     for _ in range(args.warmup):
-        oracle.chunked(q, k, v, g, beta, host["scale"], None, [0, T])
+        run()
     times = []
     for _ in range(args.steps):
         t = time.perf_counter()
-        oracle.chunked(q, k, v, g, beta, host["scale"], None, [0, T])
+        run()
         times.append(time.perf_counter() - t)
-    sec = sum(times) / len(times) * (w.hq / nk)  # seconds for the whole workload
+    sec = statistics.median(times)
     value = T / sec
-    sample = (f"chunk-form oracle (f64, OpenMP) per step over all {T} tokens of {nk}/{w.hq} q/k head groups; "
-              f"rate scaled to all {w.hv} v-heads")
+    sample = (f"chunk-form oracle (f64, OpenMP, {procs} threads) per step over the whole workload: all {T} tokens, "
+              f"all {w.hv} v-heads; median of {args.steps} timed steps")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "B": 1, "T": T, "hq": w.hq, "hv": w.hv, "dk": 128, "dv": 128, "chunk": 64},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
-                         "sample": sample},
+        "step_ms": {"median": sec * 1e3, "mean": statistics.mean(times) * 1e3, "min": min(times) * 1e3,
+                    "max": max(times) * 1e3},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": procs, "kind": "oracle", "sample": sample,
+                         "cpu": cpu_model()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -773,6 +849,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the varlen and T=65536 prefill legs")
+    ap.add_argument("--detail", action="store_true", help="full per-kernel and per-leg objects in the JSON line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -4,29 +4,41 @@
 // and returns a gdn_status; nothing is enqueued on failure. There is one
 // compute path per io dtype (f32: SIMT kernels; bf16: tensor-core kernels)
 // and no host-side fallback of any kind.
+#include <atomic>
 #include <mutex>
 
 #include "gdn_common.cuh"
+#include "tma_host.cuh"
 
 namespace gdn {
 namespace {
 
 __device__ int g_status_word;  // device status word (first device-side error)
 
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};  // limit of the prefill kernels' bounded waits
+
 constexpr int kMaxDevices = 64;
 int *g_status_ptr[kMaxDevices];
+unsigned long long g_status_ctx[kMaxDevices];  // context id the cached address belongs to
 std::mutex g_status_mu;
 
-// Device address of the status word for the current device (looked up once
-// per device; cudaGetSymbolAddress needs that device to be current).
+// Device address of the status word for the current device, looked up once
+// per device and context (cudaGetSymbolAddress needs that device current;
+// the context id catches a cudaDeviceReset, after which the module and its
+// variables are loaded anew).
 int *status_ptr() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     std::lock_guard<std::mutex> lk(g_status_mu);
-    if (!g_status_ptr[dev]) {
+    unsigned long long ctx = 0;
+    const bool have_ctx = current_context_id(&ctx);
+    if (!g_status_ptr[dev] || !have_ctx || g_status_ctx[dev] != ctx) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
         g_status_ptr[dev] = static_cast<int *>(p);
+        // the symbol lookup made the context current if it was not yet
+        g_status_ctx[dev] = (have_ctx || current_context_id(&ctx)) ? ctx : 0;
     }
     return g_status_ptr[dev];
 }
@@ -160,6 +172,7 @@ int chunk_fwd(const gdn_problem *p, const void *q, const void *k, const void *v,
     a.seq_info = reinterpret_cast<SeqInfo *>(ws + L.seq_off);
     a.chunk_info = reinterpret_cast<ChunkInfo *>(ws + L.chunk_off);
     a.status = status;
+    a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
     if (p->io_dtype == GDN_DT_BF16) {
         a.ready = prefill_tc_ready_flags(ws + L.data_off, a.max_chunks, a.hv);
         a.done = a.ready + size_t(a.max_chunks) * a.hv;  // output counters follow the ready flags
@@ -333,6 +346,13 @@ int gdn_read_device_status(void *stream, int clear) {
     if (clear && cudaMemsetAsync(status, 0, sizeof(int), s) != cudaSuccess) return GDN_ECUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ECUDA;
     return host;
+}
+
+int gdn_get_device_status(void *stream) { return gdn_read_device_status(stream, 1); }
+
+int gdn_set_wait_limit_ns(unsigned long long ns) {
+    g_wait_ns.store(ns ? ns : kDefaultWaitNs, std::memory_order_relaxed);
+    return GDN_OK;
 }
 
 }  // extern "C"

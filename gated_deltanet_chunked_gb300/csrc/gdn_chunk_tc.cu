@@ -138,7 +138,7 @@ struct PrepSmem {
     alignas(1024) uint8_t Ag[kTile];
     alignas(1024) float MX[64 * kFPitch]; // M, inverted in place into A; then A diag(beta) bf16 [i][j]
     float beta[64], gc[64], gcp[64];
-    uint64_t bar_load, bar_v, bar_mma;
+    uint64_t bar_load, bar_v, bar_mma, bar_drain;
     uint32_t tmem;
     int abort;
 };
@@ -191,7 +191,7 @@ __device__ __forceinline__ void prep_unit(const PrefillArgs &a, const TcWs &w, c
 
     // [K;Q] K^T : M=128 (rows 0-63 K K^T, rows 64-127 Q K^T), N=64, K=128
     if (tid == 0) {
-        if (mbar_wait(&s.bar_load, ld_phase)) {
+        if (mbar_wait(&s.bar_load, ld_phase, a.wait_ns)) {
             tc_fence_after();
             const uint32_t kq = smem_u32(s.KQ);
             const uint32_t id = idesc_bf16_f32(128, 64, false, false);
@@ -229,7 +229,7 @@ __device__ __forceinline__ void prep_unit(const PrefillArgs &a, const TcWs &w, c
     // (both only read the Q tile). A row scale commutes with the swizzle
     // inside the row, so the copy is linear: thread p moves bytes 16p..16p+15
     // of each 8 KiB half, and every warp writes 512 contiguous bytes.
-    if (mbar_wait(&s.bar_load, ld_phase)) {
+    if (mbar_wait(&s.bar_load, ld_phase, a.wait_ns)) {
 #pragma unroll 2
         for (int k2 = 0; k2 < 8; ++k2) {
             const int p = tid + kPrepThreads * k2, hf = p >> 9, o16 = p & 511, r = o16 >> 3;
@@ -242,7 +242,7 @@ __device__ __forceinline__ void prep_unit(const PrefillArgs &a, const TcWs &w, c
         }
     }
     // warp-uniform outcome: the tcgen05 loads below are .sync.aligned
-    const bool ok_kq = __all_sync(0xffffffffu, !s.abort && mbar_wait(&s.bar_mma, mma_phase));
+    const bool ok_kq = __all_sync(0xffffffffu, !s.abort && mbar_wait(&s.bar_mma, mma_phase, a.wait_ns));
     if (!ok_kq) s.abort = 1;
     mma_phase ^= 1;
     tc_fence_after();
@@ -436,7 +436,7 @@ __device__ __forceinline__ void prep_unit(const PrefillArgs &a, const TcWs &w, c
         mma_commit(&s.bar_mma);
     }
     ebar();
-    if (!s.abort && !mbar_wait(&s.bar_mma, mma_phase)) s.abort = 1;
+    if (!s.abort && !mbar_wait(&s.bar_mma, mma_phase, a.wait_ns)) s.abort = 1;
     mma_phase ^= 1;
     tc_fence_after();
     // free now: Ag (the W operand) and the solve buffer past A diag(beta)
@@ -472,7 +472,7 @@ __device__ __forceinline__ void prep_unit(const PrefillArgs &a, const TcWs &w, c
     // ---- U_c^T = V_c^T (A diag(beta))^T : M=128 (e), N=64 (i), K=64 (j),
     //      V tile read as an MN-major A;  K_{c-1} W_c^T : M=64 (t), N=64 (i), K=128
     if (tid == 0 && !s.abort) {
-        if (mbar_wait(&s.bar_v, ld_phase)) {
+        if (mbar_wait(&s.bar_v, ld_phase, a.wait_ns)) {
             tc_fence_after();
             const uint32_t kq = smem_u32(s.KQ), ab = smem_u32(Ab);
             const uint32_t idu = idesc_bf16_f32(128, 64, true, false);
@@ -494,7 +494,7 @@ __device__ __forceinline__ void prep_unit(const PrefillArgs &a, const TcWs &w, c
         }
     }
     ebar();
-    const bool ok_u = __all_sync(0xffffffffu, !s.abort && mbar_wait(&s.bar_mma, mma_phase));
+    const bool ok_u = __all_sync(0xffffffffu, !s.abort && mbar_wait(&s.bar_mma, mma_phase, a.wait_ns));
     if (!ok_u) s.abort = 1;
     mma_phase ^= 1;
     tc_fence_after();
@@ -544,6 +544,10 @@ __device__ __forceinline__ void prep_unit(const PrefillArgs &a, const TcWs &w, c
         record_status(a.status, GDN_ETIMEOUT);
         mbar_wait(&s.bar_load, ld_phase, 100000000ull);  // bounded drain of the tile copies
         mbar_wait(&s.bar_v, ld_phase, 100000000ull);
+        // and of the MMAs this thread issued: the commit tracks every one
+        // of them (the engine stops after an abort, so phase 0 is its only use)
+        mma_commit(&s.bar_drain);
+        mbar_wait(&s.bar_drain, 0, 100000000ull);
     }
     ld_phase ^= 1;
     // publish the unit: the plain stores of every engine thread are ordered
@@ -600,7 +604,7 @@ struct StateSmem {
     // per math warp, two staging buffers of its 32 x 32 bf16 output block
     // (rows r, 64-byte rows of e) for TMA stores
     alignas(1024) uint8_t Ost[8][2][2048];
-    uint64_t fullB[2], emptyB[2], fullM[2], emptyM[2], ready_s, ready_x, mma, mma_o;
+    uint64_t fullB[2], emptyB[2], fullM[2], emptyM[2], ready_s, ready_x, mma, mma_o, drain;
     uint32_t tmem;
     int abort;
     int outc[8];  // output gate on: chunks of this walk whose block of math warp w is in memory
@@ -638,6 +642,7 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
         mbar_init(&s.ready_x, kMathThreads / 32);
         mbar_init(&s.mma, 1);
         mbar_init(&s.mma_o, 1);
+        mbar_init(&s.drain, 1);
         for (int i = 0; i < kMathThreads / 32; ++i) s.outc[i] = 0;
         fence_mbar_init();
     }
@@ -663,7 +668,7 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
                     if (ld_acquire_gpu(w.ready + size_t(si.first_chunk + known + 1) * a.hv + h)) {
                         ++known;
                         fence_proxy_async_global();  // the bulk copies read what the flag published
-                    } else if (globaltimer_ns() - t0 > 2000000000ull) {
+                    } else if (globaltimer_ns() - t0 > a.wait_ns) {
                         return false;
                     } else {
                         __nanosleep(256);
@@ -675,7 +680,8 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
             for (int c = -1; c < nc && !s.abort; ++c) {
                 const int b = (c + 1) & 1, use = (c + 1) >> 1;
                 const bool cur = c >= 0, nxt = c + 1 < nc;
-                if (!units_ready(min(c + 1, nc - 1)) || (use > 0 && !mbar_wait(&empty[b], (use - 1) & 1))) {
+                if (!units_ready(min(c + 1, nc - 1)) ||
+                    (use > 0 && !mbar_wait(&empty[b], (use - 1) & 1, a.wait_ns))) {
                     s.abort = 1;
                     break;
                 }
@@ -727,9 +733,11 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
             const uint64_t dPc = sdesc_sw128(smem_u32(s.bs[0].Pc), 16, 1024);
             const uint64_t dB2 = sdesc_sw128(smem_u32(s.bs[0].B2), 16, 1024);
             const uint64_t dstage = uint64_t(sizeof(BStage) >> 4);
+            int released[2] = {0, 0};  // operand-release commits issued per stage
             for (int c = -1; c < nc && !s.abort; ++c) {
                 const int b = (c + 1) & 1, use = (c + 1) >> 1;
-                if (!mbar_wait_spin(&s.ready_s, (c + 1) & 1) || !mbar_wait_spin(&s.fullB[b], use & 1)) {
+                if (!mbar_wait_spin(&s.ready_s, (c + 1) & 1, a.wait_ns) ||
+                    !mbar_wait_spin(&s.fullB[b], use & 1, a.wait_ns)) {
                     s.abort = 1;
                     break;
                 }
@@ -739,7 +747,7 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
                 for (int t = 0; t < 8; ++t)  // (c) Sigma_c [-gamma_c W_{c+1} ; Q_c]^T
                     mma_bf16_ts(tmem + kTmV, tmem + kTmSA + 8 * t,
                                 dB2 + ob + (((t >> 2) * 2 * kTile + (t & 3) * 32) >> 4), id_c, t > 0);
-                if (!mbar_wait_spin(&s.ready_x, (c + 1) & 1)) {
+                if (!mbar_wait_spin(&s.ready_x, (c + 1) & 1, a.wait_ns)) {
                     s.abort = 1;
                     break;
                 }
@@ -756,14 +764,19 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
                     mma_commit(&s.mma_o);
                 }
                 mma_commit(&s.emptyB[b]);
+                ++released[b];
             }
+            // every MMA this thread issued has completed once the drain
+            // commit arrives (after an abort some were issued without a
+            // commit of their own): the tensor memory they write is freed
+            // when the CTA ends
+            mma_commit(&s.drain);
+            mbar_wait(&s.drain, 0, 100000000ull);
             // the last arrivals on the operand-release barriers come from MMA
             // completion: wait for them so that nothing lands after the next
             // walk has re-armed the barriers
-            for (int b = 0; b < 2; ++b) {
-                const int uses = (nc + 2 - b) >> 1;  // steps -1 .. nc-1 that used stage b
-                if (uses > 0) mbar_wait(&s.emptyB[b], (uses - 1) & 1, 100000000ull);
-            }
+            for (int b = 0; b < 2; ++b)
+                if (released[b] > 0) mbar_wait(&s.emptyB[b], (released[b] - 1) & 1, 100000000ull);
         }
     } else if (warp == kPublishWarp) {
         // ----------------------- output publication -------------------------
@@ -782,7 +795,7 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
                     for (int cc = published; cc < m; ++cc)
                         red_release_add_gpu(a.done + size_t(si.first_chunk + cc) * a.hv + h, kMathThreads / 32);
                     published = m;
-                } else if (globaltimer_ns() - t0 > 2000000000ull) {
+                } else if (globaltimer_ns() - t0 > a.wait_ns) {
                     s.abort = 1;
                     break;
                 } else {
@@ -847,7 +860,8 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
         // across the warp before they steer control flow
         for (int c = -1; nc > 0 && c < nc && !__any_sync(0xffffffffu, s.abort); ++c) {
             const int b = (c + 1) & 1, use = (c + 1) >> 1;
-            if (!__all_sync(0xffffffffu, mbar_wait_spin(&s.fullM[b], use & 1) && mbar_wait_spin(&s.mma, (c + 1) & 1))) {
+            if (!__all_sync(0xffffffffu, mbar_wait_spin(&s.fullM[b], use & 1, a.wait_ns) &&
+                                             mbar_wait_spin(&s.mma, (c + 1) & 1, a.wait_ns))) {
                 s.abort = 1;
                 break;
             }
@@ -856,7 +870,7 @@ __device__ __forceinline__ void state_walk(const PrefillArgs &a, const TcWs &w, 
             // O_c (from the output columns, complete once (b) is) is read
             // before the next step's (c) may overwrite those columns
             auto read_o = [&](float *o) {
-                if (!__all_sync(0xffffffffu, mbar_wait_spin(&s.mma_o, c & 1))) return false;
+                if (!__all_sync(0xffffffffu, mbar_wait_spin(&s.mma_o, c & 1, a.wait_ns))) return false;
                 tc_fence_after();
                 tmem_ld32(tmem + lrow + kTmO + 32 * ch, o);
                 tmem_ld_wait();
@@ -1011,7 +1025,7 @@ __device__ __forceinline__ bool gate_unit(const PrefillArgs &a, int c, int h, in
     if (lane == 0) {
         const uint64_t t0 = globaltimer_ns();
         while (ld_acquire_gpu(cnt) < kMathThreads / 32) {
-            if (globaltimer_ns() - t0 > 2000000000ull) {
+            if (globaltimer_ns() - t0 > a.wait_ns) {
                 ok = false;
                 break;
             }
@@ -1131,6 +1145,7 @@ k_chunk_fused_tc(FusedArgs fa, const __grid_constant__ CUtensorMap tm_q, const _
             mbar_init(&s.bar_load, 1);
             mbar_init(&s.bar_v, 1);
             mbar_init(&s.bar_mma, 1);
+            mbar_init(&s.bar_drain, 1);
             fence_mbar_init();
         }
         __syncthreads();

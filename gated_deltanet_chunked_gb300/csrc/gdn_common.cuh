@@ -53,6 +53,9 @@ struct PrefillArgs {
     const float *norm_weight;
     float norm_eps;
     int *done;        // per-unit count of math warps whose output block has landed (tensor-core path)
+    // limit of every bounded wait of the launch, in ns of wall time (2 s
+    // unless a test lowers it through gdn_set_wait_limit_ns)
+    unsigned long long wait_ns;
 };
 
 __device__ __forceinline__ void record_status(int *status, int code) {

@@ -14,10 +14,14 @@
 //
 // In host code the array's name is only a host-side stand-in, never a device
 // address. The device address is looked up once per device, with that device
-// current, by cudaGetSymbolAddress on the first call made on that device.
+// current, by cudaGetSymbolAddress on the first call made on that device, and
+// cached with the id of the context it belongs to: a cudaDeviceReset unloads
+// the module, and the first call in the new context looks the address up
+// again instead of handing the kernels a stale pointer.
 #include <mutex>
 
 #include "gdn_common.cuh"
+#include "tma_host.cuh"
 
 namespace gdn {
 namespace {
@@ -26,18 +30,22 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[GDN_NOALLOC_SCR
 
 constexpr int kMaxNoallocDevices = 64;
 void *g_scratch_addr[kMaxNoallocDevices];
+unsigned long long g_scratch_ctx[kMaxNoallocDevices];
 std::mutex g_scratch_mu;
 
 // Device address of the scratch array on the current device (set-up on the
-// first call per device; later calls only read the cached pointer).
+// first call per device and context; later calls only read the cache).
 int scratch_address(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxNoallocDevices) return GDN_ECUDA;
     std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    unsigned long long ctx = 0;
+    const bool have_ctx = current_context_id(&ctx);
+    if (!g_scratch_addr[dev] || !have_ctx || g_scratch_ctx[dev] != ctx) {
         void *ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return GDN_ECUDA;
         g_scratch_addr[dev] = ptr;
+        g_scratch_ctx[dev] = (have_ctx || current_context_id(&ctx)) ? ctx : 0;
     }
     *out = g_scratch_addr[dev];
     return GDN_OK;

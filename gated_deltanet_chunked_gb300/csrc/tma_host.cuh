@@ -24,6 +24,31 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
+// Unique id of the calling thread's current CUDA context (cuCtxGetId through
+// the driver entry point; ids are never reused within a process). Device
+// addresses of the library's __device__ variables belong to the context that
+// loaded the module, so a per-device cache of them is keyed by this id: after
+// cudaDeviceReset the next call sees a new context and looks them up again.
+// Returns false if the id cannot be read (no current context yet).
+inline bool current_context_id(unsigned long long *id) {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    CUcontext ctx = nullptr;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
 // 3-D bf16 tensor [d2][d1][d0] (d0 contiguous) with byte strides s1 (between
 // d1 rows) and s2 (between d2 slabs), copied in boxes of b0 x b1 x b2 with the
 // 128-byte swizzle; out-of-range elements read as zero.

@@ -164,10 +164,15 @@ int gdn_chunk_fwd_gated(const gdn_problem *p, const void *q, const void *k, cons
  * GDN_NOALLOC_SCRATCH_BYTES (32 MiB) that every GPU loading the library holds
  * until the process exits. No call allocates or frees anything.
  *  - Returns GDN_ETOOBIG, without launching, when
- *    gdn_chunk_fwd_workspace_size(p) > GDN_NOALLOC_SCRATCH_BYTES.
- *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture.
+ *    gdn_chunk_fwd_workspace_size(p) > GDN_NOALLOC_SCRATCH_BYTES. With the
+ *    Qwen3.5-style layer (hq = 16, hv = 32) one sequence fits up to 959
+ *    tokens on the bf16 path and 447 on the f32 path (the workspace grows by
+ *    about 2.1 MB (bf16) or 4.7 MB (f32) per 64-token chunk at hv = 32;
+ *    fewer v-heads fit proportionally more tokens). Larger prefills use
+ *    gdn_chunk_fwd with a caller workspace.
+ *  - The first call on a device (and the first after a cudaDeviceReset of
+ *    it) looks up the array's device address with cudaGetSymbolAddress, with
+ *    that device current; make that first call before any stream capture.
  *  - All calls share the one array and it keeps the last call's contents;
  *    nothing in it needs to start at zero. Calls whose work overlaps on the
  *    GPU (different streams, different host threads without ordering) race
@@ -307,6 +312,13 @@ int gdn_gating(const gdn_problem *p, const float *a, const float *b, const float
  * `clear` is non-zero. Returns GDN_ECUDA if the CUDA calls themselves fail. */
 int gdn_read_device_status(void *stream, int clear);
 
+/* The status read under the name the library's boundary was specified with:
+ * gdn_read_device_status(stream, 1). Synchronises `stream`, returns the first
+ * device-side error (GDN_ETIMEOUT, GDN_EDEVICE_INPUT) recorded since the last
+ * read, or GDN_OK, and resets the word, the way cudaGetLastError resets the
+ * runtime's last error. Returns GDN_ECUDA if the CUDA calls themselves fail. */
+int gdn_get_device_status(void *stream);
+
 /* Static, human-readable name of a gdn_status value. */
 const char *gdn_status_string(int status);
 
@@ -343,6 +355,17 @@ int gdn_profile_collect(long long *launches, double *ms, long long *timed, int c
 
 /* Static name of a gdn_kernel id. */
 const char *gdn_kernel_name(int kernel);
+
+/* Sets, process-wide, the limit of every bounded device-side wait in the
+ * prefill kernels launched after the call (the tensor-core kernel's copy,
+ * MMA and ready-flag waits), in nanoseconds of wall time; 0 restores the
+ * default of 2 s. A wait that runs out records GDN_ETIMEOUT in the device
+ * status word; the kernel then drains what it has in flight (copies and
+ * MMAs, each drain bounded too), frees its tensor memory and returns, so the
+ * context stays usable and the call's outputs are unspecified. Meant for
+ * tests of that path: a limit of a few microseconds makes the waits on
+ * not-yet-prepared chunks run out. Returns GDN_OK. */
+int gdn_set_wait_limit_ns(unsigned long long ns);
 
 #ifdef __cplusplus
 }

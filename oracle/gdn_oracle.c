@@ -46,6 +46,28 @@ int gdn_oracle_max_threads(void) {
 #endif
 }
 
+/* Threads for the following calls (n <= 0: leave as is); returns the count
+ * now in effect. Timing only: the results do not depend on it, since every
+ * (sequence, head) pair is computed by one thread in a fixed order. */
+int gdn_oracle_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}
+
+/* Processors the OpenMP runtime sees on this host. */
+int gdn_oracle_num_procs(void) {
+#ifdef _OPENMP
+    return omp_get_num_procs();
+#else
+    return 1;
+#endif
+}
+
 /* ---------------------------------------------------------------------------
  * Recurrent form, token by token ("Lab3 GDN Prefill", Gated DeltaNet section).
  * For each token t of a sequence, with alpha_t = exp(g_t):

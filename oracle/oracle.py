@@ -72,6 +72,10 @@ def _load():
             lib.gdn_oracle_chunked.restype = None
             lib.gdn_oracle_max_threads.argtypes = []
             lib.gdn_oracle_max_threads.restype = ctypes.c_int
+            lib.gdn_oracle_set_threads.argtypes = [ctypes.c_int]
+            lib.gdn_oracle_set_threads.restype = ctypes.c_int
+            lib.gdn_oracle_num_procs.argtypes = []
+            lib.gdn_oracle_num_procs.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -79,6 +83,17 @@ def _load():
 def max_threads() -> int:
     """OpenMP threads the oracle will use (1 if built without OpenMP)."""
     return int(_load().gdn_oracle_max_threads())
+
+
+def set_threads(n: int) -> int:
+    """Sets the OpenMP threads of later calls (for timing; results do not
+    depend on it) and returns the count in effect."""
+    return int(_load().gdn_oracle_set_threads(int(n)))
+
+
+def num_procs() -> int:
+    """Processors the oracle's OpenMP runtime sees on this host."""
+    return int(_load().gdn_oracle_num_procs())
 
 
 def _f64(x):

@@ -35,6 +35,60 @@ def check(x, ref, io_dtype, what):
     return err
 
 
+def check_f32_state(x, ref, what):
+    """An f32-arithmetic result (the decode step's f32 state, whatever the io
+    dtype: bf16 inputs are widened exactly) at the f32 bar, element by
+    element: max|x - ref| / max|ref| <= 1e-4."""
+    x = x.detach().cpu().double().numpy() if hasattr(x, "detach") else x
+    assert np.all(np.isfinite(x)), f"{what}: non-finite values"
+    err = max_rel(x, ref)
+    assert err <= F32_MAX_REL, f"{what}: max_rel {err:.3e} > {F32_MAX_REL}"
+    return err
+
+
+# round-to-nearest into bf16 (8 significant bits) moves a value by at most
+# 2^-8 of its magnitude
+BF16_HALF_ULP = 2.0 ** -8
+
+
+def check_bf16_rounded(x, ref, what):
+    """A bf16 output of f32 arithmetic, element by element: every element
+    within its own rounding bound, |x - ref| <= 2^-8 |ref| plus the f32 bar
+    (1e-4 of the largest magnitude) for the arithmetic before the rounding."""
+    x = x.detach().cpu().double().numpy() if hasattr(x, "detach") else np.asarray(x, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert np.all(np.isfinite(x)), f"{what}: non-finite values"
+    bound = BF16_HALF_ULP * np.abs(ref) * (1 + 1e-3) + F32_MAX_REL * max(float(np.max(np.abs(ref))), 1e-30)
+    excess = np.abs(x - ref) / bound
+    worst = np.unravel_index(int(np.argmax(excess)), excess.shape)
+    assert excess[worst] <= 1.0, (f"{what}: element {worst} off by {abs(x[worst] - ref[worst]):.3e} "
+                                  f"(ref {ref[worst]:.3e}, bound {bound[worst]:.3e})")
+    return float(excess[worst])
+
+
+def check_per_head(x, ref, cu, io_dtype, what):
+    """check() applied to every (sequence, head) slice of a packed [T, H, d]
+    output (cu = offsets [N+1]) or of a [N, H, dk, dv] state (cu None), so
+    that a wrong chunk of one sequence or one bad head is not diluted by the
+    rest of the tensor. Returns the worst error."""
+    x = x.detach().cpu().double().numpy() if hasattr(x, "detach") else np.asarray(x, np.float64)
+    ref = np.asarray(ref, np.float64)
+    worst = 0.0
+    if cu is None:
+        for n in range(x.shape[0]):
+            for h in range(x.shape[1]):
+                worst = max(worst, check(x[n, h], ref[n, h], io_dtype, f"{what} [seq {n}, head {h}]"))
+    else:
+        cu = [int(c) for c in (cu.tolist() if hasattr(cu, "tolist") else cu)]
+        for n in range(len(cu) - 1):
+            if cu[n + 1] == cu[n]:
+                continue
+            for h in range(x.shape[1]):
+                worst = max(worst, check(x[cu[n]:cu[n + 1], h], ref[cu[n]:cu[n + 1], h], io_dtype,
+                                         f"{what} [seq {n}, head {h}]"))
+    return worst
+
+
 def to_dev(inp, dev):
     return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
 

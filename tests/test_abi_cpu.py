@@ -204,3 +204,60 @@ def test_binding_rejects_wrong_dtypes():
         gdn.gdn_causal_conv1d_silu(torch.zeros((2, 512), dtype=bf), torch.zeros((512, 4), dtype=bf), 1, 2)
     with pytest.raises(ValueError):
         gdn.gdn_gating(g, g, torch.zeros(2, dtype=torch.float64), torch.zeros(2))
+
+
+def test_binding_rejects_wrong_shapes_before_any_call():
+    """Shapes are checked against the problem descriptor in the binding: a
+    wrong final_state, state or gate shape never reaches the library (where it
+    would be an out-of-bounds write)."""
+    import torch
+
+    bf = torch.bfloat16
+    T, hq, hv = 70, 1, 2
+    q = torch.zeros((T, hq, 128), dtype=bf)
+    v = torch.zeros((T, hv, 128), dtype=bf)
+    g = torch.zeros((T, hv))
+    cu = torch.tensor([0, T], dtype=torch.int32)
+    with pytest.raises(ValueError, match="final_state"):
+        gdn.gdn_chunk_fwd(q, q, v, g, g, 0.1, cu_seqlens=cu, final_state=torch.zeros((1, hv, 128, 64)))
+    with pytest.raises(ValueError, match="initial_state"):
+        gdn.gdn_chunk_fwd(q, q, v, g, g, 0.1, cu_seqlens=cu, initial_state=torch.zeros((2, hv, 128, 128)))
+    with pytest.raises(ValueError, match="beta"):
+        gdn.gdn_chunk_fwd(q, q, v, g, g[:, :1].contiguous(), 0.1, cu_seqlens=cu)
+    with pytest.raises(ValueError, match="out"):
+        gdn.gdn_chunk_fwd(q, q, v, g, g, 0.1, cu_seqlens=cu, out=torch.zeros((T, hv, 64), dtype=bf))
+    with pytest.raises(ValueError, match="state"):
+        gdn.gdn_recurrent_step(q[:4], q[:4], v[:4], g[:4], g[:4], 0.1, torch.zeros((4, hv, 128, 64)))
+    with pytest.raises(ValueError, match="state_indices"):
+        gdn.gdn_recurrent_step(q[:4], q[:4], v[:4], g[:4], g[:4], 0.1, torch.zeros((4, hv, 128, 128)),
+                               state_indices=torch.zeros(3, dtype=torch.int32))
+    with pytest.raises(ValueError, match="weight"):
+        gdn.gdn_gated_rmsnorm(v, v, torch.ones(64), 1e-6)
+
+
+def test_binding_rejects_host_tensors():
+    """Correctly shaped tensors that are not on a CUDA device are refused in
+    the binding (the kernels would dereference their host addresses)."""
+    import torch
+
+    bf = torch.bfloat16
+    T, hq, hv = 70, 1, 2
+    q = torch.zeros((T, hq, 128), dtype=bf)
+    v = torch.zeros((T, hv, 128), dtype=bf)
+    g = torch.zeros((T, hv))
+    with pytest.raises(ValueError, match="CUDA"):
+        gdn.gdn_chunk_fwd(q, q, v, g, g, 0.1, cu_seqlens=torch.tensor([0, T], dtype=torch.int32))
+    with pytest.raises(ValueError, match="CUDA"):
+        gdn.gdn_recurrent_step(q[:4], q[:4], v[:4], g[:4], g[:4], 0.1, torch.zeros((4, hv, 128, 128)))
+    with pytest.raises(ValueError, match="CUDA"):
+        gdn.gdn_gated_rmsnorm(v, v, torch.ones(128), 1e-6)
+
+
+def test_boundary_names_of_the_specification():
+    """The boundary's specified names resolve in the library: the two prefill
+    entry points, the workspace query, the decode step, the status word
+    (gdn_get_device_status) and the status strings."""
+    lib = gdn.load()
+    for name in ("gdn_chunk_fwd", "gdn_chunk_fwd_workspace_size", "gdn_recurrent_step", "gdn_get_device_status",
+                 "gdn_status_string"):
+        assert hasattr(lib, name), name

@@ -5,6 +5,11 @@ The 256-sequence x 32-head workload is checked in full on its first step and
 over 100 consecutive steps on a sample of sequences; small cases cover both
 io dtypes, slot indirection with padding slots, gate inputs on both sides of
 the +-20 softplus branches, saturated sigmoids and zero q/k rows.
+
+The kernel's arithmetic is f32 throughout, so an f32 state is held to the f32
+bar (max_rel <= 1e-4, element by element) whatever the io dtype; bf16 outputs
+are held to their rounding bound element by element. Only the bf16 state
+cache of the SGLang precision mode is compared normwise.
 """
 import numpy as np
 import pytest
@@ -12,7 +17,7 @@ import torch
 
 import oracle
 from gated_deltanet_chunked_gb300 import gdn, workloads as W
-from parity_util import check, to_dev
+from parity_util import check, check_bf16_rounded, check_f32_state, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -41,7 +46,8 @@ def test_gated_decode_first_step_full(cuda):
     assert gdn.gdn_read_device_status() == gdn.GDN_OK
     o_ref, st_ref = step_ref(inp, A_log, dt_bias, state0)
     check(o, o_ref, torch.bfloat16, "o")
-    check(state, st_ref, torch.bfloat16, "state")
+    check_bf16_rounded(o, o_ref, "o")
+    check_f32_state(state, st_ref, "state")
 
 
 def test_gated_decode_100_steps_sampled(cuda):
@@ -56,8 +62,8 @@ def test_gated_decode_100_steps_sampled(cuda):
         sub = {k: (v[sample] if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
         o_ref, st_ref = step_ref(sub, A_log, dt_bias, st_ref)
         if step in (0, 9, 49, 99):
-            check(o[sample], o_ref, torch.bfloat16, f"o step {step}")
-    check(state[sample], st_ref, torch.bfloat16, "state after 100 steps")
+            check_bf16_rounded(o[sample], o_ref, f"o step {step}")
+    check_f32_state(state[sample], st_ref, "state after 100 steps")
 
 
 def _small_case(dtype, N=6, hq=2, hv=4, a_sigma=1.0, seed=41):
@@ -86,7 +92,7 @@ def test_gated_slots_padding_and_softplus_branches(cuda, dtype):
     o_ref, st_ref = step_ref(inp, A_log, dt_bias, state0, idx.numpy())
     live = [0, 2, 3, 5]
     check(o[live], o_ref[live], dtype, "o")
-    check(state, st_ref, dtype, "state")
+    check_f32_state(state, st_ref, "state")
     assert torch.all(o[[1, 4]] == 5.0)
     untouched = [1, 2, 4, 6, 7]
     assert torch.equal(state[untouched], state0[untouched].to(cuda))
@@ -104,7 +110,7 @@ def test_gated_zero_rows(cuda, dtype):
     o_ref, st_ref = step_ref(inp, A_log, dt_bias, state0)
     assert torch.all(o[1] == 0)
     check(o[[0, 2]], o_ref[[0, 2]], dtype, "o")
-    check(state, st_ref, dtype, "state")
+    check_f32_state(state, st_ref, "state")
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
@@ -120,7 +126,9 @@ def test_gated_many_steps_small(cuda, dtype):
         o = step_gpu(inp, A_log, dt_bias, state, cuda)
         o_ref, st_ref = step_ref(inp, A_log, dt_bias, st_ref)
         check(o, o_ref, dtype, f"o step {step}")
-    check(state, st_ref, dtype, "state after 40 steps")
+        if dtype == torch.bfloat16:
+            check_bf16_rounded(o, o_ref, f"o step {step}")
+    check_f32_state(state, st_ref, "state after 40 steps")
 
 
 def test_gated_invalid_arguments(cuda):
@@ -154,7 +162,9 @@ def test_gated_decode_with_output_gate(cuda, dtype):
     y_ref = oracle.gated_rmsnorm(o_ref, z, weight, 1e-6)
     live = [0, 1, 3, 4, 5]
     check(out[live], y_ref[live], dtype, "y")
-    check(state, st_ref, dtype, "state")
+    if dtype == torch.bfloat16:
+        check_bf16_rounded(out[live], y_ref[live], "y")
+    check_f32_state(state, st_ref, "state")
     assert torch.all(out[2] == 7.0)
 
 
@@ -169,8 +179,10 @@ def test_gated_decode_full_with_output_gate(cuda):
                                      d["scale"], state, z=z.to(cuda), norm_weight=weight.to(cuda), norm_eps=1e-6)
     torch.cuda.synchronize()
     o_ref, st_ref = step_ref(inp, A_log, dt_bias, state0)
-    check(y, oracle.gated_rmsnorm(o_ref, z, weight, 1e-6), torch.bfloat16, "y")
-    check(state, st_ref, torch.bfloat16, "state")
+    y_ref = oracle.gated_rmsnorm(o_ref, z, weight, 1e-6)
+    check(y, y_ref, torch.bfloat16, "y")
+    check_bf16_rounded(y, y_ref, "y")
+    check_f32_state(state, st_ref, "state")
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])

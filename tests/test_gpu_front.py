@@ -15,7 +15,7 @@ import torch
 
 import oracle
 from gated_deltanet_chunked_gb300 import gdn, workloads as W
-from parity_util import check
+from parity_util import check, check_f32_state
 
 pytestmark = pytest.mark.gpu
 
@@ -211,6 +211,10 @@ def test_decode_layer_core_from_projections(cuda, state_bf16):
     idx = torch.tensor([3, 0, 4, 1, 2], dtype=torch.int32)
     cst, S = cst0.to(cuda), S0.to(cuda)
     cst_ref, S_ref = cst0.double().numpy(), S0.double().numpy()
+    # the recurrent step alone, fed the q/k/v the GPU's conv step produced:
+    # its f32 state is held to the f32 bar (the chain above it carries the
+    # bf16 rounding of the conv outputs and is compared normwise)
+    S_step = S0.double().numpy()
     cu = np.arange(N + 1)
     rng = np.random.default_rng(82)
     for step in range(8):
@@ -229,6 +233,10 @@ def test_decode_layer_core_from_projections(cuda, state_bf16):
         o_r, S_ref = oracle.recurrent_step_gated(q_r, k_r, v_r, a, bb, A_log, dt_bias, 128 ** -0.5, S_ref, idx.numpy(),
                                                  beta_bf16=state_bf16, state_bf16=state_bf16)
         check(y, oracle.gated_rmsnorm(o_r, z, nw, 1e-6), dtype, f"y step {step}")
+        _, S_step = oracle.recurrent_step_gated(q.cpu(), k.cpu(), v.cpu(), a, bb, A_log, dt_bias, 128 ** -0.5, S_step, idx.numpy(),
+                                                beta_bf16=state_bf16, state_bf16=state_bf16)
     assert gdn.gdn_read_device_status() == gdn.GDN_OK
     check(S, S_ref, dtype, "recurrent state after 8 steps")
+    if not state_bf16:
+        check_f32_state(S, S_step, "recurrent state after 8 steps (step kernel alone)")
     check(cst, cst_ref, dtype, "conv state after 8 steps")
