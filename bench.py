@@ -731,12 +731,20 @@ def run_front_end(args, dev, world, peaks, peak_src):
 
 
 def cpu_model():
-    """The host CPU's model name (from /proc/cpuinfo; Arm hosts may list only
-    implementer/part numbers) and the processor count."""
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, where Arm hosts
+    list only implementer/part numbers) and the processor count."""
     name = None
     try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() == "Model name":
+                name = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
         with open("/proc/cpuinfo") as f:
-            info = f.read()
+            info = f.read() if name is None else ""
         for key in ("model name", "Model name", "Hardware", "CPU part"):
             for line in info.splitlines():
                 if line.split(":")[0].strip() == key:
@@ -746,6 +754,9 @@ def cpu_model():
                 break
     except OSError:
         pass
+    arm_parts = {"0xd4f": "Arm Neoverse-V2", "0xd40": "Arm Neoverse-V1", "0xd0c": "Arm Neoverse-N1",
+                 "0xd49": "Arm Neoverse-N2"}
+    name = arm_parts.get(name, name)
     return {"model": name or "unknown", "nproc": os.cpu_count()}
 
 
