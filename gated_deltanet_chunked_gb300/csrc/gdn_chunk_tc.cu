@@ -166,7 +166,7 @@ __device__ __forceinline__ void prep_unit(const PrefillArgs &a, const TcWs &w, c
     // scratch in the Ag region, all consumed before Ag is written
     float *graw = reinterpret_cast<float *>(s.Ag);  // [64] gates of chunk c
     float *gpraw = graw + 64;                       // [64] gates of chunk c-1
-    float *T = graw + 128;                          // [3][256] block products of the solve
+    float *T = graw + 128;                          // [4][256] per-warp scratch of the solve
 
     if (tid == 0) {
         mbar_arrive_expect_tx(&s.bar_load, (has_prev ? 6u : 4u) * kTile);
@@ -328,62 +328,30 @@ __device__ __forceinline__ void prep_unit(const PrefillArgs &a, const TcWs &w, c
         for (int ii = 0; ii < 16; ++ii) M[(16 * b + ii) * kFPitch + 16 * b + jj] = x[ii];
     }
     ebar();
-    // off-diagonal blocks by anti-diagonal levels, the blocks of a level in
-    // parallel:  level 1: (1,0) (2,1) (3,2);  level 2: (2,0) (3,1);  level 3: (3,0)
+    // off-diagonal blocks by anti-diagonal levels, one warp per block of a
+    // level, on warp-level tensor-core MMAs (tf32 operands, f32 accumulate):
+    //   level 1: (1,0) (2,1) (3,2);  level 2: (2,0) (3,1);  level 3: (3,0)
     //   T_ij = sum_{k=j}^{i-1} L_ik X_kj,   X_ij = -X_ii T_ij
     // X_ij (i > j) goes to the mirror block (j, i) of the strict upper
     // triangle (zero until now), because later levels still read the
-    // original L blocks below the diagonal.
+    // original L blocks below the diagonal. No block of a level reads what
+    // another block of the same level writes.
     {
-        const int ii = tid >> 3, jj = 2 * (tid & 7);  // two adjacent outputs per thread and block
-        auto xblk = [&](int k, int j) -> const float * {  // X_kj, k >= j
-            return k == j ? M + (16 * k) * kFPitch + 16 * k : M + (16 * j) * kFPitch + 16 * k;
-        };
+        auto blk = [&](int r, int c) { return M + (16 * r) * kFPitch + 16 * c; };
+        float *Tw = T + 256 * warp;  // this warp's 16x16 scratch (pitch 16)
 #pragma unroll
         for (int lev = 1; lev <= 3; ++lev) {
-            const int nb = 4 - lev;  // blocks (j + lev, j), j = 0 .. nb-1
-#pragma unroll
-            for (int j = 0; j < nb; ++j) {
-                const int i = j + lev;
-                float t0 = 0.f, t1 = 0.f;
-#pragma unroll
-                for (int k = j; k < i; ++k) {
-                    const float4 *Lr = reinterpret_cast<const float4 *>(M + (16 * i + ii) * kFPitch + 16 * k);
-                    const float *Xc = xblk(k, j) + jj;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float4 lq = Lr[q];
-                        const float2 x0 = *reinterpret_cast<const float2 *>(Xc + (4 * q + 0) * kFPitch);
-                        const float2 x1 = *reinterpret_cast<const float2 *>(Xc + (4 * q + 1) * kFPitch);
-                        const float2 x2 = *reinterpret_cast<const float2 *>(Xc + (4 * q + 2) * kFPitch);
-                        const float2 x3 = *reinterpret_cast<const float2 *>(Xc + (4 * q + 3) * kFPitch);
-                        t0 = fmaf(lq.x, x0.x, t0); t1 = fmaf(lq.x, x0.y, t1);
-                        t0 = fmaf(lq.y, x1.x, t0); t1 = fmaf(lq.y, x1.y, t1);
-                        t0 = fmaf(lq.z, x2.x, t0); t1 = fmaf(lq.z, x2.y, t1);
-                        t0 = fmaf(lq.w, x3.x, t0); t1 = fmaf(lq.w, x3.y, t1);
-                    }
-                }
-                *reinterpret_cast<float2 *>(&T[j * 256 + ii * 16 + jj]) = make_float2(t0, t1);
-            }
-            ebar();
-#pragma unroll
-            for (int j = 0; j < nb; ++j) {
-                const int i = j + lev;
-                const float4 *Xr = reinterpret_cast<const float4 *>(M + (16 * i + ii) * kFPitch + 16 * i);
-                float o0 = 0.f, o1 = 0.f;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 xq = Xr[q];  // X_ii row (zero above the diagonal)
-                    const float2 u0 = *reinterpret_cast<const float2 *>(&T[j * 256 + (4 * q + 0) * 16 + jj]);
-                    const float2 u1 = *reinterpret_cast<const float2 *>(&T[j * 256 + (4 * q + 1) * 16 + jj]);
-                    const float2 u2 = *reinterpret_cast<const float2 *>(&T[j * 256 + (4 * q + 2) * 16 + jj]);
-                    const float2 u3 = *reinterpret_cast<const float2 *>(&T[j * 256 + (4 * q + 3) * 16 + jj]);
-                    o0 = fmaf(xq.x, u0.x, o0); o1 = fmaf(xq.x, u0.y, o1);
-                    o0 = fmaf(xq.y, u1.x, o0); o1 = fmaf(xq.y, u1.y, o1);
-                    o0 = fmaf(xq.z, u2.x, o0); o1 = fmaf(xq.z, u2.y, o1);
-                    o0 = fmaf(xq.w, u3.x, o0); o1 = fmaf(xq.w, u3.y, o1);
-                }
-                *reinterpret_cast<float2 *>(M + (16 * j + ii) * kFPitch + 16 * i + jj) = make_float2(-o0, -o1);
+            if (warp < 4 - lev) {  // warp-uniform: block (warp + lev, warp)
+                const int j = warp, i = j + lev;
+                float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int k = j; k < i; ++k)  // X_kj: the diagonal block in place, else its mirror (j, k)
+                    mma_block16(t0, t1, blk(i, k), kFPitch, k == j ? blk(j, j) : blk(j, k), kFPitch);
+                store_block16(Tw, 16, t0, t1);
+                __syncwarp();
+                float x0[4] = {0.f, 0.f, 0.f, 0.f}, x1[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_block16(x0, x1, blk(i, i), kFPitch, Tw, 16, /*negate_x=*/true);
+                store_block16(blk(j, i), kFPitch, x0, x1);
+                __syncwarp();  // the scratch is rewritten at the next level
             }
             ebar();
         }

@@ -344,6 +344,59 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r) {
 // Waits until this thread's tcgen05.st writes have landed in TMEM.
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// ---------------------------------------------------------------------------
+// warp-level MMA (mma.sync m16n8k8, tf32 inputs, f32 accumulate): for the
+// small 16x16 block products of the triangular solve, where a tensor-memory
+// round trip would cost more than the product. Fragment layouts (PTX ISA,
+// m16n8k8 .tf32), with g = lane / 4 and t = lane % 4:
+//   A (16x8, row-major):  a0 = A[g][t], a1 = A[g+8][t], a2 = A[g][t+4], a3 = A[g+8][t+4]
+//   B (8x8, column):      b0 = B[t][g], b1 = B[t+4][g]
+//   C, D (16x8):          d0 = C[g][2t], d1 = C[g][2t+1], d2 = C[g+8][2t], d3 = C[g+8][2t+1]
+// ---------------------------------------------------------------------------
+// nearest tf32 value of x (10-bit significand, ties away from zero), as the
+// 32-bit pattern the MMA reads
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+// d += A * B on one warp (all 32 lanes, converged)
+__device__ __forceinline__ void mma_tf32_m16n8k8(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// D (16x16, two 16x8 column halves d0 | d1) += X * Y for 16x16 f32 blocks X
+// (row pitch px) and Y (row pitch py) in shared memory; `negate_x` uses -X.
+__device__ __forceinline__ void mma_block16(float (&d0)[4], float (&d1)[4], const float *X, int px, const float *Y,
+                                            int py, bool negate_x = false) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const float sx = negate_x ? -1.f : 1.f;
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+        const int k0 = 8 * ks;
+        const uint32_t a[4] = {to_tf32(sx * X[g * px + k0 + t]), to_tf32(sx * X[(g + 8) * px + k0 + t]),
+                               to_tf32(sx * X[g * px + k0 + t + 4]), to_tf32(sx * X[(g + 8) * px + k0 + t + 4])};
+        const uint32_t b0[2] = {to_tf32(Y[(k0 + t) * py + g]), to_tf32(Y[(k0 + t + 4) * py + g])};
+        const uint32_t b1[2] = {to_tf32(Y[(k0 + t) * py + 8 + g]), to_tf32(Y[(k0 + t + 4) * py + 8 + g])};
+        mma_tf32_m16n8k8(d0, a, b0);
+        mma_tf32_m16n8k8(d1, a, b1);
+    }
+}
+
+// stores the 16x16 accumulator (d0 | d1) to f32 shared memory (row pitch p)
+__device__ __forceinline__ void store_block16(float *Z, int p, const float (&d0)[4], const float (&d1)[4]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    *reinterpret_cast<float2 *>(Z + g * p + 2 * t) = make_float2(d0[0], d0[1]);
+    *reinterpret_cast<float2 *>(Z + (g + 8) * p + 2 * t) = make_float2(d0[2], d0[3]);
+    *reinterpret_cast<float2 *>(Z + g * p + 8 + 2 * t) = make_float2(d1[0], d1[1]);
+    *reinterpret_cast<float2 *>(Z + (g + 8) * p + 8 + 2 * t) = make_float2(d1[2], d1[3]);
+}
+
 // TMEM address of (lane, column): lane in bits 16-31, column in bits 0-15.
 __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint32_t col) {
     return base + (lane << 16) + col;
