@@ -277,48 +277,145 @@ __global__ void __launch_bounds__(kCThreads) k_conv1d_silu(ConvArgs a) {
     }
 }
 
-// One token per sequence (decode): block (n, channel block); the token's x
-// and the sequence's slot are read at once, then the three state rows.
+// One token per sequence (decode). A thread owns 8 consecutive channels (one
+// 16-byte access per row for bf16) of kStepSeqs sequences: the CTA reads its
+// channels' weights and bias once, then issues the x rows and (after the slot
+// indices) the three state rows of all its sequences before any arithmetic,
+// so that a thread has a dozen independent loads in flight instead of one
+// dependent chain per sequence.
+constexpr int kStepCh = 8;
+constexpr int kStepThreads = 128;                          // 1024 channels per CTA
+constexpr int kStepSeqs = 4;
+
+// 8 consecutive values of a row as loaded (one 16-byte access for bf16, two
+// for f32), widened to f32 only when used, so that the loads in flight hold
+// as few registers as possible
 template <typename T>
-__global__ void __launch_bounds__(kCThreads) k_conv1d_step(ConvArgs a) {
-    const int n = blockIdx.x;
-    const int c0 = blockIdx.y * kCPerBlock + threadIdx.x * kCPerThread;
-    if (c0 >= a.C) return;  // whole warps
+struct Row8;
+template <>
+struct Row8<__nv_bfloat16> {
+    uint4 u;
+    __device__ __forceinline__ void zero() { u = make_uint4(0, 0, 0, 0); }
+    __device__ __forceinline__ void load(const __nv_bfloat16 *p) { u = *reinterpret_cast<const uint4 *>(p); }
+    __device__ __forceinline__ void store(__nv_bfloat16 *p) const { *reinterpret_cast<uint4 *>(p) = u; }
+    __device__ __forceinline__ float get(int i) const {
+        const uint32_t w = i < 2 ? u.x : i < 4 ? u.y : i < 6 ? u.z : u.w;
+        return __uint_as_float((i & 1) ? (w & 0xffff0000u) : (w << 16));
+    }
+};
+template <>
+struct Row8<float> {
+    float4 a, b;
+    __device__ __forceinline__ void zero() { a = b = make_float4(0.f, 0.f, 0.f, 0.f); }
+    __device__ __forceinline__ void load(const float *p) {
+        a = reinterpret_cast<const float4 *>(p)[0];
+        b = reinterpret_cast<const float4 *>(p)[1];
+    }
+    __device__ __forceinline__ void store(float *p) const {
+        reinterpret_cast<float4 *>(p)[0] = a;
+        reinterpret_cast<float4 *>(p)[1] = b;
+    }
+    __device__ __forceinline__ float get(int i) const {
+        const float4 &v = i < 4 ? a : b;
+        const int j = i & 3;
+        return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+    }
+};
+
+template <typename T>
+__device__ __forceinline__ void st8(T *p, const float (&v)[8]);
+template <>
+__device__ __forceinline__ void st8<float>(float *p, const float (&v)[8]) {
+    reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+template <>
+__device__ __forceinline__ void st8<__nv_bfloat16>(__nv_bfloat16 *p, const float (&v)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
+        w[q] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kStepThreads) k_conv1d_step(ConvArgs a) {
+    const int n0 = blockIdx.x * kStepSeqs;
+    const int c0 = blockIdx.y * (kStepThreads * kStepCh) + threadIdx.x * kStepCh;
+    // heads are 128 channels = 16 threads, so a head is wholly valid or not;
+    // invalid threads still join the half-warp reductions below
+    const bool cvalid = c0 < a.C;
     const T *X = static_cast<const T *>(a.x);
     T *S = static_cast<T *>(a.state);
-    int slot = S ? (a.idx ? a.idx[n] : n) : -1;
-    const float4 xv = ld4v<T>(X + size_t(n) * a.C + c0);
-    float4 r[kCPerThread];
+    int slot[kStepSeqs];
 #pragma unroll
-    for (int i = 0; i < kCPerThread; ++i) r[i] = reinterpret_cast<const float4 *>(a.weight)[c0 + i];
-    const float4 bias = a.bias ? *reinterpret_cast<const float4 *>(a.bias + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
-    if (slot >= a.slots) {
-        if ((threadIdx.x & 31) == 0) record_status(a.status, GDN_EDEVICE_INPUT);
-        slot = -1;
+    for (int k = 0; k < kStepSeqs; ++k) {
+        const int n = n0 + k;
+        slot[k] = (n < a.N && S) ? (a.idx ? a.idx[n] : n) : -1;
     }
-    float4 h[kConvK - 1];
+    Row8<T> xv[kStepSeqs];
 #pragma unroll
-    for (int j = 0; j < kConvK - 1; ++j)
-        h[j] = slot >= 0 ? ld4v<T>(S + (size_t(slot) * (kConvK - 1) + j) * a.C + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 y;
-    y.x = silu_f(fmaf(r[0].w, xv.x, fmaf(r[0].z, h[2].x, fmaf(r[0].y, h[1].x, fmaf(r[0].x, h[0].x, bias.x)))));
-    y.y = silu_f(fmaf(r[1].w, xv.y, fmaf(r[1].z, h[2].y, fmaf(r[1].y, h[1].y, fmaf(r[1].x, h[0].y, bias.y)))));
-    y.z = silu_f(fmaf(r[2].w, xv.z, fmaf(r[2].z, h[2].z, fmaf(r[2].y, h[1].z, fmaf(r[2].x, h[0].z, bias.z)))));
-    y.w = silu_f(fmaf(r[3].w, xv.w, fmaf(r[3].z, h[2].w, fmaf(r[3].y, h[1].w, fmaf(r[3].x, h[0].w, bias.w)))));
+    for (int k = 0; k < kStepSeqs; ++k) {
+        xv[k].zero();
+        if (cvalid && n0 + k < a.N) xv[k].load(X + size_t(n0 + k) * a.C + c0);
+    }
+    float4 w[8];
+    float bias[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        w[i] = cvalid ? reinterpret_cast<const float4 *>(a.weight)[c0 + i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        bias[i] = (cvalid && a.bias) ? a.bias[c0 + i] : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < kStepSeqs; ++k) {
+        if (slot[k] >= a.slots) {
+            if (threadIdx.x == 0 && blockIdx.y == 0) record_status(a.status, GDN_EDEVICE_INPUT);
+            slot[k] = -1;
+        }
+    }
+    Row8<T> h[kStepSeqs][kConvK - 1];
+#pragma unroll
+    for (int k = 0; k < kStepSeqs; ++k)
+#pragma unroll
+        for (int j = 0; j < kConvK - 1; ++j) {
+            h[k][j].zero();
+            if (cvalid && slot[k] >= 0) h[k][j].load(S + (size_t(slot[k]) * (kConvK - 1) + j) * a.C + c0);
+        }
     const int qk_c = a.hq * kHeadDim;
-    if (a.norm_qk && c0 < 2 * qk_c) {  // uniform over the warp (one head)
-        float ss = y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
-        for (int m = 16; m; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-        const float inv = rsqrtf(ss + 1e-6f);
-        y.x *= inv; y.y *= inv; y.z *= inv; y.w *= inv;
-    }
-    if (c0 < qk_c) st4v<T>(static_cast<T *>(a.oq) + size_t(n) * qk_c + c0, y);
-    else if (c0 < 2 * qk_c) st4v<T>(static_cast<T *>(a.ok) + size_t(n) * qk_c + c0 - qk_c, y);
-    else st4v<T>(static_cast<T *>(a.ov) + size_t(n) * a.hv * kHeadDim + c0 - 2 * qk_c, y);
-    if (slot >= 0) {  // the window moves on by one input
-        st4v<T>(S + (size_t(slot) * (kConvK - 1) + 0) * a.C + c0, h[1]);
-        st4v<T>(S + (size_t(slot) * (kConvK - 1) + 1) * a.C + c0, h[2]);
-        st4v<T>(S + (size_t(slot) * (kConvK - 1) + 2) * a.C + c0, xv);
+    const bool norm = a.norm_qk && c0 < 2 * qk_c;  // uniform over a head (16 threads)
+#pragma unroll
+    for (int k = 0; k < kStepSeqs; ++k) {
+        const int n = n0 + k;
+        float y[8];
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            // taps oldest first: w.x x[t-3], w.y x[t-2], w.z x[t-1], w.w x[t]
+            y[i] = silu_f(fmaf(w[i].w, xv[k].get(i),
+                               fmaf(w[i].z, h[k][2].get(i),
+                                    fmaf(w[i].y, h[k][1].get(i), fmaf(w[i].x, h[k][0].get(i), bias[i])))));
+            ss = fmaf(y[i], y[i], ss);
+        }
+        // sum over the head's 16 threads (lanes of one half-warp)
+#pragma unroll
+        for (int m = 8; m; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+        if (!cvalid || n >= a.N) continue;
+        if (norm) {
+            const float inv = rsqrtf(ss + 1e-6f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) y[i] *= inv;
+        }
+        if (c0 < qk_c) st8<T>(static_cast<T *>(a.oq) + size_t(n) * qk_c + c0, y);
+        else if (c0 < 2 * qk_c) st8<T>(static_cast<T *>(a.ok) + size_t(n) * qk_c + c0 - qk_c, y);
+        else st8<T>(static_cast<T *>(a.ov) + size_t(n) * a.hv * kHeadDim + c0 - 2 * qk_c, y);
+        if (slot[k] >= 0) {  // the window moves on by one input
+            T *srow = S + size_t(slot[k]) * (kConvK - 1) * a.C + c0;
+            h[k][1].store(srow);
+            h[k][2].store(srow + a.C);
+            xv[k].store(srow + 2 * size_t(a.C));
+        }
     }
 }
 
@@ -375,10 +472,11 @@ cudaError_t launch_conv1d_step(const gdn_problem &p, const void *x, const float 
     if (p.num_seqs == 0) return cudaSuccess;
     ConvArgs a{x, weight, bias, conv_state, state_indices, nullptr, out_q, out_k, out_v,
                p.num_seqs, C, p.num_seqs, p.num_state_slots, p.hq, p.hv, 1, norm_qk, 1, status};
-    const dim3 grid(p.num_seqs, (C + kCPerBlock - 1) / kCPerBlock);
+    const int per_block = kStepThreads * kStepCh;
+    const dim3 grid((p.num_seqs + kStepSeqs - 1) / kStepSeqs, (C + per_block - 1) / per_block);
     LaunchScope scope(GDN_K_CONV1D_STEP, s);
-    if (p.io_dtype == GDN_DT_BF16) k_conv1d_step<__nv_bfloat16><<<grid, kCThreads, 0, s>>>(a);
-    else k_conv1d_step<float><<<grid, kCThreads, 0, s>>>(a);
+    if (p.io_dtype == GDN_DT_BF16) k_conv1d_step<__nv_bfloat16><<<grid, kStepThreads, 0, s>>>(a);
+    else k_conv1d_step<float><<<grid, kStepThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
