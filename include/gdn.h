@@ -172,7 +172,7 @@ int gdn_chunk_fwd_gated(const gdn_problem *p, const void *q, const void *k, cons
  *    gdn_chunk_fwd with a caller workspace.
  *  - The first call on a device (and the first after a cudaDeviceReset of
  *    it) looks up the array's device address with cudaGetSymbolAddress, with
- *    that device current; make that first call before any stream capture.
+ *    that device current; later calls reuse the address.
  *  - All calls share the one array and it keeps the last call's contents;
  *    nothing in it needs to start at zero. Calls whose work overlaps on the
  *    GPU (different streams, different host threads without ordering) race
