@@ -6,7 +6,8 @@ Element-by-element comparison on seeded inputs:
     taken per (sequence, v-head) slice of o and per (sequence, v-head) state,
     so that one wrong tail chunk or one bad walk is not diluted by the rest.
 Small cases span several chunks and ragged tails (lengths 1, 63, 64, 65, ...),
-empty sequences, GVA groups 1/2/4 and present/absent initial states. The
+empty sequences, GVA groups 1/2/4/8, present/absent initial states and a
+batch of 64 short prompts. The
 full-size workloads are checked in the launch configuration the benchmark
 times: T=4096 in full, varlen and T=65536 on sampled q/k head groups that the
 oracle computes independently.
@@ -106,6 +107,21 @@ def test_bit_reproducible_and_permutation_invariant(cuda):
     o3, S3 = run_gpu_prefill(inp2, cuda)
     assert torch.equal(o3, cat(o1.cpu()).to(cuda))
     assert torch.equal(S3, S1[perm])
+
+
+@pytest.mark.parametrize("dtype,hq,hv", [(torch.float32, 2, 4), (torch.bfloat16, 16, 32)], ids=["f32", "bf16"])
+def test_many_short_sequences(cuda, dtype, hq, hv):
+    # a serving-style packed batch: 64 prompts of 1..300 tokens with initial
+    # states; at Hv = 32 the 2048 walks queue 64 deep on each walk CTA, and the
+    # chunk table maps every chunk to its sequence by search
+    lengths = [int(L) for L in W.varlen_lengths(np.random.Generator(np.random.PCG64(77)), 64, 1, 300)]
+    inp = W.make_custom_prefill(4242, lengths, hq, hv, dtype, s0_sigma=0.05)
+    o, S = run_gpu_prefill(inp, cuda)
+    o_ref, S_ref = oracle_prefill(inp)
+    check(o, o_ref, dtype, "o")
+    check(S, S_ref, dtype, "final_state")
+    check_per_head(o, o_ref, inp["cu_seqlens"], dtype, "o")
+    check_per_head(S, S_ref, None, dtype, "final_state")
 
 
 def test_no_final_state(cuda):
