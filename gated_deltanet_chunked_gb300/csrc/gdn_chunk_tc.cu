@@ -1157,10 +1157,12 @@ size_t prefill_tc_workspace(int max_chunks, int hv) {
 int *prefill_tc_ready_flags(void *ws_data, int max_chunks, int hv) { return tc_carve(ws_data, max_chunks, hv).ready; }
 
 // CTAs that walk: the split that minimises the larger of the two estimated
-// times, with the chunks of a sequence estimated from the mean length.
-// Measured at T=4096: a walk step ~1.4 us, ~5 us per walk beyond its steps,
-// ~14 us until the first chunks are prepared, an engine unit ~17 us with
-// three engines busy on an SM.
+// times, with the chunks of a sequence estimated from the mean length (the
+// lengths themselves are on the device). Measured at T=4096 and on packed
+// batches: ~13 us until the first chunks are prepared, a walk step ~1.32 us,
+// ~4 us per walk beyond its steps, a round of units (one per engine, three
+// engines on an SM) ~12 us in the steady state. Walks are dealt round-robin,
+// so a walk CTA carries walks / n of them on average (at least one).
 static int state_ctas(const PrefillArgs &a, int ctas) {
     const int walks = a.num_seqs * a.hv;
     const double steps = double(a.total_tokens) / (double(kChunk) * (a.num_seqs > 0 ? a.num_seqs : 1)) + 2.0;
@@ -1168,8 +1170,9 @@ static int state_ctas(const PrefillArgs &a, int ctas) {
     int best = 1;
     double best_t = 1e300;
     for (int n = 1; n < ctas && n <= walks; ++n) {
-        const double t_walk = 14.0 + double((walks + n - 1) / n) * (steps * 1.4 + 5.0);
-        const double t_prep = std::ceil(units / (double(ctas - n) * kEngines)) * 17.0;
+        const double per_cta = double(walks) / n;
+        const double t_walk = 13.0 + (per_cta > 1.0 ? per_cta : 1.0) * (steps * 1.32 + 4.0);
+        const double t_prep = std::ceil(units / (double(ctas - n) * kEngines)) * 12.0;
         const double t = t_walk > t_prep ? t_walk : t_prep;
         if (t < best_t) {
             best_t = t;
