@@ -23,8 +23,11 @@
 // thread, so that a whole tile is in flight per CTA without holding
 // registers (loads issued token by token left the kernel bound by load
 // latency at 0.3 of HBM); tiles may span several sequences (the window
-// restarts from each sequence's state). A token that is a whole sequence
-// (decode) finds its sequence without a search.
+// restarts from each sequence's state). The copies also bring the K-1 rows
+// before the tile, the history of a tile that starts inside a sequence: as
+// plain loads issued after the tile's copies they arrived after the whole
+// tile. A token that is a whole sequence (decode) finds its sequence without
+// a search.
 // In-place state update without a race: a tile never starts at the second or
 // third token of a sequence (its start moves to the fourth), so the old state
 // of a sequence is read only by the thread that processes the sequence's
@@ -111,6 +114,15 @@ __global__ void __launch_bounds__(kCThreads) k_conv1d_silu(ConvArgs a) {
     const int32_t one_seq[2] = {0, a.T};
     const int32_t *cu = a.cu ? a.cu : one_seq;
     const int N = a.cu ? a.N : 1;
+    const bool active = c0 < a.C;  // whole warps: C is a multiple of 128
+    // the taps and bias first: their loads then overlap the tile bounds'
+    // dependent reads of cu_seqlens instead of queueing behind the tile's copies
+    float4 wr[kCPerThread], bias = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (active) {
+#pragma unroll
+        for (int i = 0; i < kCPerThread; ++i) wr[i] = reinterpret_cast<const float4 *>(a.weight)[c0 + i];
+        if (a.bias) bias = *reinterpret_cast<const float4 *>(a.bias + c0);
+    }
     if (a.cu) {  // the offsets must start at 0, never decrease and end at T
         bool bad = false;
         for (int i = threadIdx.x; i < N; i += kCThreads) bad |= cu[i] > cu[i + 1];
@@ -125,36 +137,31 @@ __global__ void __launch_bounds__(kCThreads) k_conv1d_silu(ConvArgs a) {
     const int t_end = tile_start(cu, N, a.T, min(t_nominal + a.tile, a.T));
     if (t_begin >= t_end) return;  // uniform over the CTA
     const T *X = static_cast<const T *>(a.x);
-    // the tile's rows of x for these 1024 channels, by bulk copies (one per token)
+    // the tile's rows of x for these 1024 channels and the K-1 rows before it
+    // (a mid-sequence tile's history), by bulk copies (one per token)
+    const int h_begin = max(t_begin - (kConvK - 1), 0);
     const int cb0 = cblock * kCPerBlock;
     const uint32_t row_bytes = uint32_t(min(kCPerBlock, a.C - cb0)) * sizeof(T);
     if (threadIdx.x == 0) {
         mbar_init(&bar, 1);
         abort_flag = 0;
         fence_mbar_init();
-        mbar_arrive_expect_tx(&bar, uint32_t(t_end - t_begin) * row_bytes);
-        for (int t = t_begin; t < t_end; ++t)
-            bulk_load(xs_raw + size_t(t - t_begin) * kCPerBlock * sizeof(T), X + size_t(t) * a.C + cb0, row_bytes,
+        mbar_arrive_expect_tx(&bar, uint32_t(t_end - h_begin) * row_bytes);
+        for (int t = h_begin; t < t_end; ++t)
+            bulk_load(xs_raw + size_t(t - h_begin) * kCPerBlock * sizeof(T), X + size_t(t) * a.C + cb0, row_bytes,
                       &bar);
     }
     __syncthreads();
-    const bool active = c0 < a.C;  // whole warps: C is a multiple of 128
     T *S = static_cast<T *>(a.state);
     if (!active) {  // still waits for the copies into this CTA's shared memory
         if (threadIdx.x == 0 && !mbar_wait(&bar, 0)) record_status(a.status, GDN_ETIMEOUT);
         return;
     }
     float4 w[kConvK];  // w[j] = taps j of the 4 channels
-    {
-        float4 r[kCPerThread];
-#pragma unroll
-        for (int i = 0; i < kCPerThread; ++i) r[i] = reinterpret_cast<const float4 *>(a.weight)[c0 + i];
-        w[0] = make_float4(r[0].x, r[1].x, r[2].x, r[3].x);
-        w[1] = make_float4(r[0].y, r[1].y, r[2].y, r[3].y);
-        w[2] = make_float4(r[0].z, r[1].z, r[2].z, r[3].z);
-        w[3] = make_float4(r[0].w, r[1].w, r[2].w, r[3].w);
-    }
-    const float4 bias = a.bias ? *reinterpret_cast<const float4 *>(a.bias + c0) : make_float4(0.f, 0.f, 0.f, 0.f);
+    w[0] = make_float4(wr[0].x, wr[1].x, wr[2].x, wr[3].x);
+    w[1] = make_float4(wr[0].y, wr[1].y, wr[2].y, wr[3].y);
+    w[2] = make_float4(wr[0].z, wr[1].z, wr[2].z, wr[3].z);
+    w[3] = make_float4(wr[0].w, wr[1].w, wr[2].w, wr[3].w);
     // taps and bias as channel pairs (0, 1) and (2, 3) for the packed f32x2 arithmetic
     float2 wl[kConvK], wh[kConvK];
 #pragma unroll
@@ -169,6 +176,7 @@ __global__ void __launch_bounds__(kCThreads) k_conv1d_silu(ConvArgs a) {
     else dst = static_cast<T *>(a.ov), dcol = c0 - 2 * qk_c, drow = a.hv * kHeadDim;
     const bool norm = a.norm_qk && c0 < 2 * qk_c;  // uniform over the warp (one head)
 
+    const T *XS = reinterpret_cast<const T *>(xs_raw) + threadIdx.x * kCPerThread;
     int s = seq_of(cu, N, t_begin);
     int s_end = cu[s + 1];
     float4 h0, h1, h2;  // x_{t-3}, x_{t-2}, x_{t-1}
@@ -187,7 +195,10 @@ __global__ void __launch_bounds__(kCThreads) k_conv1d_silu(ConvArgs a) {
 #pragma unroll
         for (int i = 0; i < kConvK - 1; ++i) {
             const int j = p + i;  // index in [state ; x of the sequence]
-            if (j >= kConvK - 1) e[i] = ld4v<T>(X + size_t(ss + j - (kConvK - 1)) * a.C + c0);
+            const int row = ss + j - (kConvK - 1);  // token of an x entry
+            if (j >= kConvK - 1)
+                e[i] = row >= h_begin ? ld4v<T>(XS + size_t(row - h_begin) * kCPerBlock)  // copied with the tile
+                                      : ld4v<T>(X + size_t(row) * a.C + c0);
             else if (slot >= 0) e[i] = ld4v<T>(S + (size_t(slot) * (kConvK - 1) + j) * a.C + c0);
             else e[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
@@ -255,13 +266,16 @@ __global__ void __launch_bounds__(kCThreads) k_conv1d_silu(ConvArgs a) {
         for (int j = 0; j < 4; ++j) st4v<T>(dst + size_t(t + j) * drow + dcol, y[j]);
         h0 = x1, h1 = x2, h2 = x3;
     };
-    load_history(t_begin);
+    // a tile at a sequence's start takes its history from the conv state (plain
+    // loads, issued before the wait); a mid-sequence tile from the copied rows
+    const bool at_start = t_begin == cu[s];
+    if (at_start) load_history(t_begin);
     const bool landed = mbar_wait(&bar, 0);
     if (!__all_sync(0xffffffffu, landed)) {
         if (lane == 0) record_status(a.status, GDN_ETIMEOUT);
         return;
     }
-    const T *XS = reinterpret_cast<const T *>(xs_raw) + threadIdx.x * kCPerThread;
+    if (!at_start) load_history(t_begin);
     for (int t = t_begin; t < t_end;) {
         if (t == s_end) {  // next non-empty sequence starts here
             while (cu[s + 1] <= t) ++s;
@@ -270,10 +284,10 @@ __global__ void __launch_bounds__(kCThreads) k_conv1d_silu(ConvArgs a) {
         }
         const int run_end = min(t_end, s_end);  // tokens of sequence s in this tile
         for (; t + 4 <= run_end; t += 4) {
-            const T *xr = XS + size_t(t - t_begin) * kCPerBlock;
+            const T *xr = XS + size_t(t - h_begin) * kCPerBlock;
             emit4(t, ld4v<T>(xr), ld4v<T>(xr + kCPerBlock), ld4v<T>(xr + 2 * kCPerBlock), ld4v<T>(xr + 3 * kCPerBlock));
         }
-        for (; t < run_end; ++t) emit(t, ld4v<T>(XS + size_t(t - t_begin) * kCPerBlock));
+        for (; t < run_end; ++t) emit(t, ld4v<T>(XS + size_t(t - h_begin) * kCPerBlock));
     }
 }
 
@@ -449,7 +463,8 @@ cudaError_t launch_conv1d_silu(const gdn_problem &p, const void *x, const float 
     const int max_tile = kMaxTileBytes / (kCPerBlock * esize);  // 32 (bf16) or 16 (f32)
     int tile = 1;
     while (tile < max_tile && int64_t(tile) * 2 * 3 * sms <= int64_t(p.total_tokens) * cblocks) tile *= 2;
-    const size_t smem = size_t(tile + kConvK - 2) * kCPerBlock * esize;  // a tile may grow by two rows
+    // a tile may grow by two rows and takes the K-1 rows before it
+    const size_t smem = size_t(tile + kConvK - 2 + kConvK - 1) * kCPerBlock * esize;
     const void *fn = p.io_dtype == GDN_DT_BF16 ? reinterpret_cast<const void *>(k_conv1d_silu<__nv_bfloat16>)
                                                : reinterpret_cast<const void *>(k_conv1d_silu<float>);
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
