@@ -17,7 +17,7 @@
 // k_conv1d_silu: a thread owns 4 consecutive channels (one 8- or 16-byte
 // access per token), so a warp covers exactly one 128-channel head and the
 // q/k norm is one warp reduction. A CTA (linear grid, the channel block
-// varying fastest) takes 1024 channels over a tile of tokens of the packed token axis
+// varying fastest) takes 512 channels over a tile of tokens of the packed token axis
 // and slides the window down it in registers. The tile's rows of x (2 KiB per
 // token for bf16) come into shared memory by bulk copies issued at once by one
 // thread, so that a whole tile is in flight per CTA without holding
@@ -40,10 +40,10 @@ namespace gdn {
 namespace {
 
 constexpr int kConvK = 4;  // taps
-constexpr int kCThreads = 256;
+constexpr int kCThreads = 128;
 constexpr int kCPerThread = 4;
-constexpr int kCPerBlock = kCThreads * kCPerThread;  // 1024 channels
-constexpr int kMaxTileBytes = 64 * 1024;            // x rows staged per CTA (plus two rows)
+constexpr int kCPerBlock = kCThreads * kCPerThread;  // 512 channels
+constexpr int kMaxTileBytes = 16 * 1024;            // x rows staged per CTA (plus five rows)
 
 template <typename T>
 __device__ __forceinline__ float4 ld4v(const T *p);
@@ -104,7 +104,7 @@ __device__ __forceinline__ int tile_start(const int32_t *cu, int N, int T, int t
 template <typename T>
 __global__ void __launch_bounds__(kCThreads) k_conv1d_silu(ConvArgs a) {
     using namespace tc;
-    extern __shared__ __align__(128) uint8_t xs_raw[];  // the tile's rows of x: [rows][1024] T
+    extern __shared__ __align__(128) uint8_t xs_raw[];  // the tile's rows of x: [rows][512] T
     __shared__ uint64_t bar;
     __shared__ int abort_flag;
     const int lane = threadIdx.x & 31;
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kCThreads) k_conv1d_silu(ConvArgs a) {
     const int t_end = tile_start(cu, N, a.T, min(t_nominal + a.tile, a.T));
     if (t_begin >= t_end) return;  // uniform over the CTA
     const T *X = static_cast<const T *>(a.x);
-    // the tile's rows of x for these 1024 channels and the K-1 rows before it
+    // the tile's rows of x for these 512 channels and the K-1 rows before it
     // (a mid-sequence tile's history), by bulk copies (one per token)
     const int h_begin = max(t_begin - (kConvK - 1), 0);
     const int cb0 = cblock * kCPerBlock;
@@ -456,11 +456,13 @@ cudaError_t launch_conv1d_silu(const gdn_problem &p, const void *x, const float 
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    // tokens per tile (a power of two, 1 .. 64): the largest that still gives
-    // about four CTAs per SM
+    // tokens per tile (a power of two, up to 16 for bf16): the largest that
+    // still gives at least six CTAs per SM over the grid (128-thread CTAs on
+    // 16-token tiles measured best: their load and compute phases interleave
+    // across the SM's CTAs)
     const int cblocks = (C + kCPerBlock - 1) / kCPerBlock;
     const int esize = p.io_dtype == GDN_DT_BF16 ? 2 : 4;
-    const int max_tile = kMaxTileBytes / (kCPerBlock * esize);  // 32 (bf16) or 16 (f32)
+    const int max_tile = kMaxTileBytes / (kCPerBlock * esize);  // 16 (bf16) or 8 (f32)
     int tile = 1;
     while (tile < max_tile && int64_t(tile) * 2 * 3 * sms <= int64_t(p.total_tokens) * cblocks) tile *= 2;
     // a tile may grow by two rows and takes the K-1 rows before it
