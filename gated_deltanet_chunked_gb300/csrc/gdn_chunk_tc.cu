@@ -1160,7 +1160,7 @@ int *prefill_tc_ready_flags(void *ws_data, int max_chunks, int hv) { return tc_c
 // times, with the chunks of a sequence estimated from the mean length (the
 // lengths themselves are on the device). Measured at T=4096 and on packed
 // batches: ~13 us until the first chunks are prepared, a walk step ~1.32 us,
-// ~4 us per walk beyond its steps, a round of units (one per engine, three
+// ~4 us per walk beyond its steps, a batch of units (one per engine, three
 // engines on an SM) ~12 us in the steady state. Walks are dealt round-robin,
 // so a walk CTA carries walks / n of them on average (at least one).
 static int state_ctas(const PrefillArgs &a, int ctas) {
